@@ -1,0 +1,20 @@
+"""fp64 CPU oracle for MLA decode with matrix absorption.
+
+TEST INFRASTRUCTURE ONLY.  Nothing in the product path imports this
+package: only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline /
+reference arms of ``bench.py`` use it.  It shares no code with the CUDA
+library (no kernels, headers, helpers or constants).
+
+Modules
+-------
+``oracle.mla``         the decode step written out as its plain definition
+                       (un-absorbed: K and V are reconstructed per cached token)
+``oracle.upstream``    down-projection and RoPE, used only to synthesise the
+                       inputs of the tiny fp32 workload
+``oracle.accounting``  closed-form cache sizes and FLOP counts
+
+Every function is pinned by ``tests/test_oracle_*.py`` to numbers the pages
+print, to closed forms, or to textbook special cases.
+"""
+
+from . import accounting, mla, upstream  # noqa: F401
