@@ -1,0 +1,493 @@
+"""Benchmark of one MLA decode step (append + absorb + decode + out-proj).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload v2]
+    python bench.py --impl reference ...     # the fp64 CPU oracle, timed
+
+Default workload: the DeepSeek-V2-shaped paged decode (H=128, d_h=128,
+d_c=512, d_r=64, B=64, seqlen 8192, Hq=1, block 64, permuted block table),
+seeded synthetic data.  Prints ONE JSON line on rank 0.
+
+Timing: W untimed warm-up steps, then K steps.  Before every timed step L2
+is flushed by writing a 256 MiB buffer (outside the step's events); each
+step is timed with CUDA events on the stream the library launches on.  The
+mla_decode call is also timed on its own: that is the kernel the roofline
+fraction describes.  N > 1 (torchrun): every rank runs its own replica of
+the workload (weak scaling, no collective on the data path); rank 0 reports
+the max over ranks and the whole-job throughput.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "MLA decode TFLOP/s + latent-cache GB/s, fraction of 1×B300 roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+L2_FLUSH_BYTES = 256 << 20
+
+
+# ---------------------------------------------------------------------------
+# algorithmic work (the method's own counts, not the kernels')
+# ---------------------------------------------------------------------------
+
+
+def visible_tokens(seqlens, Hq):
+    """sum over sequences and query slots of the visible cache length."""
+    s = np.asarray(seqlens, np.int64)
+    return int(sum(np.maximum(0, s - Hq + i + 1).sum() for i in range(Hq)))
+
+
+def decode_work(w, seqlens):
+    """FLOPs and bytes of mla_decode: QK^T over d_c + d_r and P C over d_c
+    per visible (token, query slot) and head; bytes are the cache rows read
+    once per sequence plus q_lat/q_rope in and o_lat/lse out."""
+    vt = visible_tokens(seqlens, w.Hq)
+    flops = 2 * w.H * (w.d_c + w.d_r) * vt + 2 * w.H * w.d_c * vt
+    cache_tokens = int(np.asarray(seqlens, np.int64).sum())
+    rows = len(seqlens) * w.Hq * w.H
+    bytes_ = cache_tokens * (w.d_c + w.d_r) * 2 + rows * (w.d_c + w.d_r) * 2 + rows * (w.d_c * 2 + 4)
+    return flops, bytes_
+
+
+def gemm_work(w, B):
+    rows = B * w.Hq
+    flops = 2 * rows * w.H * w.d_h * w.d_c
+    bytes_ = w.H * w.d_h * w.d_c * 2 + rows * w.H * (w.d_h + w.d_c) * 2
+    return flops, bytes_
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+        time.sleep(0.25)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+
+def setup_inputs(name, device, batch=None):
+    inp = synth.make_bf16_inputs(name, B_override=batch)
+    dev = {k: (v.to(device) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    return inp, dev
+
+
+def run_ours(args, rank, world, device):
+    import mla_latent_kv_74_b300 as mla
+
+    w = synth.WORKLOADS[args.workload]
+    inp, dev = setup_inputs(args.workload, device, args.batch)
+    w = inp["workload"]
+    B = w.B
+    seqlens = inp["seqlens"].numpy()
+    max_seqlen = int(seqlens.max())
+    dims = mla.Dims(H=w.H, d_h=w.d_h, d_c=w.d_c, d_r=w.d_r, block_size=w.block_size,
+                    dtype=torch.bfloat16)
+    cache = dev["cache"]
+    q_lat = torch.empty(B, w.Hq, w.H, w.d_c, dtype=torch.bfloat16, device=device)
+    o_lat = torch.empty_like(q_lat)
+    lse = torch.empty(B, w.Hq, w.H, dtype=torch.float32, device=device)
+    out = torch.empty(B, w.Hq, w.H, w.d_h, dtype=torch.bfloat16, device=device)
+    ws = mla.alloc_workspace(B, w.Hq, max_seqlen, dims, device=device)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def step(x):
+        mla.mla_append_cache(cache, inp["num_blocks"], x["block_table"], x["seqlens"],
+                             x["c_kv_new"], x["k_r_new"], dims, stream)
+        mla.mla_absorb_query(x["q_nope"], dev["W_UK"], q_lat, dims, stream)
+        ev[1].record(stream)
+        mla.mla_decode(q_lat, x["q_rope"], cache, inp["num_blocks"], x["block_table"],
+                       x["seqlens"], max_seqlen, dims, o_lat, lse, ws, stream)
+        ev[2].record(stream)
+        mla.mla_out_proj(o_lat, dev["W_UV"], out, dims, stream)
+
+    # ---- device-resident timing -------------------------------------------
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    for _ in range(args.warmup):
+        flush.zero_()
+        step(dev)
+    torch.cuda.synchronize()
+    status = mla.mla_get_error(ws)
+    if status != 0:
+        raise RuntimeError(f"device error after warm-up: {mla.status_string(status)}")
+
+    step_ms, dec_ms = [], []
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(smi_index(device.index)) as clocks:
+        t_wall = time.perf_counter()
+        for _ in range(args.steps):
+            flush.zero_()
+            ev[0].record(stream)
+            step(dev)
+            ev[3].record(stream)
+            ev[3].synchronize()
+            step_ms.append(ev[0].elapsed_time(ev[3]))
+            dec_ms.append(ev[1].elapsed_time(ev[2]))
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    if world > 1:
+        torch.distributed.barrier()
+    status = mla.mla_get_error(ws)
+    if status != 0:
+        raise RuntimeError(f"device error in the timed region: {mla.status_string(status)}")
+
+    # ---- end to end through host buffers ------------------------------------
+    host_keys = ("q_nope", "q_rope", "c_kv_new", "k_r_new", "block_table", "seqlens")
+    pinned = {k: inp[k].pin_memory() for k in host_keys}
+    staged = {k: torch.empty_like(dev[k]) for k in host_keys}
+    out_host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    h2d = sum(pinned[k].numel() * pinned[k].element_size() for k in host_keys)
+    d2h = out_host.numel() * out_host.element_size()
+    e2e_ms = []
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for it in range(args.warmup + args.steps):
+        flush.zero_()
+        e0.record(stream)
+        for k in host_keys:
+            staged[k].copy_(pinned[k], non_blocking=True)
+        step(staged)
+        out_host.copy_(out, non_blocking=True)
+        e1.record(stream)
+        e1.synchronize()
+        if it >= args.warmup:
+            e2e_ms.append(e0.elapsed_time(e1))
+
+    # ---- reduce over ranks ----------------------------------------------------
+    t_step = float(np.mean(step_ms))
+    t_dec = float(np.mean(dec_ms))
+    t_e2e = float(np.mean(e2e_ms))
+    if world > 1:
+        t = torch.tensor([t_step, t_dec, t_e2e], dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        t_step, t_dec, t_e2e = t.tolist()
+    if rank != 0:
+        return None
+
+    dflops, dbytes = decode_work(w, seqlens)
+    gflops, gbytes = gemm_work(w, B)
+    step_flops = dflops + 2 * gflops
+    peaks, peak_src = load_peaks()
+    hbm = peaks["hbm_gbs"]
+    tc_burst = peaks["bf16_tflops"]
+    dec_gbs = dbytes / (t_dec * 1e-3) / 1e9
+    dec_tflops = dflops / (t_dec * 1e-3) / 1e12
+    t_roof = max(dbytes / (hbm * 1e9), dflops / (tc_burst * 1e12))
+    bound = "hbm" if dbytes / (hbm * 1e9) >= dflops / (tc_burst * 1e12) else "tensor"
+    achieved, peak, unit = (dec_gbs, hbm, "GB/s") if bound == "hbm" else (dec_tflops, tc_burst,
+                                                                         "TFLOP/s")
+    value = world * step_flops / (t_step * 1e-3) / 1e12
+    launches_per_step = 1 + 1 + decode_launches(mla, dims, w) + 1
+    traffic = load_traffic(args.workload)
+    res = {
+        "metric": METRIC,
+        "value": round(value, 3),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(t_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) latents/queries, N(0,1/512) weights; no trained weights)",
+        "config": {
+            "workload": synth.DESCRIPTIONS[args.workload]
+            + ("" if args.batch is None else f" (batch overridden to {B})"),
+            "name": args.workload,
+            "B": B, "Hq": w.Hq, "H": w.H, "d_h": w.d_h, "d_c": w.d_c, "d_r": w.d_r,
+            "block_size": w.block_size,
+            "seqlen": int(max_seqlen) if w.seqlen else "ragged",
+            "visible_tokens": visible_tokens(seqlens, w.Hq),
+            "step": "append + absorb + decode(split-KV + combine) + out_proj",
+            "l2": "flushed before every timed step (256 MiB write outside the step's events)",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+        },
+        "decode": {
+            "ms": round(t_dec, 5),
+            "tflops": round(dec_tflops, 2),
+            "cache_gbs": round(dec_gbs, 1),
+            "roofline_time_ms": round(t_roof * 1e3, 5),
+            "roofline_time_frac": round(t_roof / (t_dec * 1e-3), 4),
+            "tensor_frac_of_burst": round(dec_tflops / tc_burst, 4),
+            "tensor_frac_of_sustained": round(dec_tflops / peaks["bf16_tflops_sustained"], 4),
+            "algorithmic_flops": dflops,
+            "algorithmic_bytes": dbytes,
+        },
+        "roofline": {
+            "kernel": "mla_decode",
+            "bound": bound,
+            "achieved": round(achieved, 2),
+            "peak": peak,
+            "unit": unit,
+            "frac": round(achieved / peak, 4),
+            "peak_source": f"{peak_src} ({'burst' if bound == 'tensor' else 'copy'})",
+            "traffic": traffic,
+        },
+        "e2e": {
+            "value": round(world * step_flops / (t_e2e * 1e-3) / 1e12, 3),
+            "unit": "TFLOP/s",
+            "ms_per_step": round(t_e2e, 5),
+            "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h),
+        },
+        "gpu_launches": int(launches_per_step * args.steps),
+        "clocks": clocks.summary(),
+        "wall_s_timed_region": round(t_wall, 3),
+    }
+    return res
+
+
+def smi_index(local_index):
+    """nvidia-smi's name for a CUDA device index (honours CUDA_VISIBLE_DEVICES)."""
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        ids = [v.strip() for v in vis.split(",") if v.strip()]
+        if local_index < len(ids):
+            return ids[local_index]
+    return str(local_index)
+
+
+def decode_launches(mla, dims, w):
+    """Kernels one mla_decode call launches on this path."""
+    return 2
+
+
+def load_traffic(name):
+    """DRAM bytes of the decode kernel from the committed ncu summary, when it
+    was captured on the current kernel version (else null)."""
+    p = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(name)
+    return e if e else None
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (cpu_baseline, and the reference arm)
+# ---------------------------------------------------------------------------
+
+
+def oracle_cores():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [p["num_threads"] for p in threadpool_info() if p.get("internal_api") == "openblas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return len(os.sched_getaffinity(0))
+
+
+def time_oracle_sample(name, budget_s, heads_per_chunk=8, inputs=None):
+    """Run the fp64 oracle on (sequence, head) rows of the workload until
+    ``budget_s`` seconds have passed; returns (algorithmic flops, seconds,
+    description)."""
+    from oracle import mla as omla
+
+    w = synth.WORKLOADS[name]
+    if inputs is None:
+        inputs = synth.make_bf16_inputs(name)
+    W_UK = inputs["W_UK"].double().numpy()
+    W_UV = inputs["W_UV"].double().numpy()
+    bs = w.block_size
+    flops = 0
+    rows = 0
+    t0 = time.perf_counter()
+    b = 0
+    done = False
+    while not done:
+        n = int(inputs["seqlens"][b])
+        nblk = -(-n // bs)
+        cache = inputs["cache"][inputs["block_table"][b, :nblk].long()].double().numpy()
+        table = np.arange(nblk)[None, :]
+        for h0 in range(0, w.H, heads_per_chunk):
+            hs = list(range(h0, min(w.H, h0 + heads_per_chunk)))
+            omla.mla_decode(inputs["q_nope"][b:b + 1].double().numpy(),
+                            inputs["q_rope"][b:b + 1].double().numpy(), cache, table,
+                            inputs["seqlens"][b:b + 1].numpy(), W_UK, W_UV, w.Hq,
+                            head_indices=hs)
+            vt = visible_tokens([n], w.Hq)
+            flops += len(hs) * (2 * (w.d_c + w.d_r) + 2 * w.d_c) * vt
+            rows += len(hs) * w.Hq
+            if time.perf_counter() - t0 >= budget_s:
+                done = True
+                break
+        b = (b + 1) % w.B
+    dt = time.perf_counter() - t0
+    return flops, dt, f"{rows} (sequence, head) rows of the {name} workload"
+
+
+def run_reference(args, rank):
+    if rank != 0:
+        return None
+    w = synth.WORKLOADS[args.workload]
+    inputs = synth.make_bf16_inputs(args.workload)
+    times, flops_all = [], []
+    desc = ""
+    for it in range(args.warmup + args.steps):
+        fl, dt, desc = time_oracle_sample(args.workload, args.ref_step_s, inputs=inputs)
+        if it >= args.warmup:
+            times.append(dt)
+            flops_all.append(fl)
+    value = sum(flops_all) / sum(times) / 1e12
+    cores = oracle_cores()
+    return {
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOP/s",
+        "impl": "reference",
+        "n_gpus": 1,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(1e3 * float(np.mean(times)), 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": synth.DESCRIPTIONS[args.workload], "name": args.workload},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"each step: {desc} (~{args.ref_step_s:.0f} s of fp64 "
+                                   f"un-absorbed oracle on the host)"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+# ---------------------------------------------------------------------------
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="v2", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the workload's batch size (small profiling captures)")
+    ap.add_argument("--cpu-baseline-s", type=float, default=15.0,
+                    help="seconds of oracle work for the cpu_baseline key (0 = skip)")
+    ap.add_argument("--ref-step-s", type=float, default=3.0,
+                    help="seconds of oracle work per step of the reference arm")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        res = run_reference(args, rank)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    res = run_ours(args, rank, world, device)
+    if res is not None:
+        if args.cpu_baseline_s > 0:
+            fl, dt, desc = time_oracle_sample(args.workload, args.cpu_baseline_s)
+            res["cpu_baseline"] = {
+                "value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": oracle_cores(),
+                "kind": "oracle",
+                "sample": f"{desc}; {dt:.1f} s of the fp64 un-absorbed oracle on the host",
+            }
+        else:
+            res["cpu_baseline"] = None
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,171 @@
+/*
+ * mla.h -- C ABI of the MLA decode library (Multi-head Latent Attention with
+ * matrix absorption), built for NVIDIA B300 (sm_103a).
+ *
+ * One decode step is four stream-ordered calls:
+ *
+ *   mla_append_cache   write the new tokens' [c_KV ; k_R] rows into the cache
+ *   mla_absorb_query   q_lat = W_UK^T q_nope            (per head)
+ *   mla_decode         softmax((q_lat.c_j + q_rope.k_R_j) * scale) over the
+ *                      cached latents, accumulated in latent space:
+ *                      o_lat = sum_j p_j c_j, plus lse
+ *   mla_out_proj       out = W_UV o_lat                  (per head)
+ *
+ * The per-head keys W_UK c_j and values W_UV c_j of cached tokens are never
+ * formed.  Sources (page title, section):
+ *   - "Multi-Head Latent Attention: Low-Rank KV Compression, Decoupled RoPE,
+ *     and Matrix Absorption": MLA (k = W^UK c, v = W^UV c, W in R^{d_h x d_c})
+ *     and Matrix Absorption.
+ *   - "MLA, dim by dim" 4.2 (decode order: absorb the query, contract the
+ *     cache last, expand with W_UV after the latent sum) and 5.2 (decoupled
+ *     RoPE: score = content + positional term, joint scale 1/sqrt(d_k+d_r),
+ *     one rotated k_R per token shared by all heads).
+ *   - "From Vanilla Transformers to Modern LLMs -- Part 3" 3.e.2 (absorbed
+ *     query), 3.g/3.p (values in latent space), 3.o (scale), 3.q (cache).
+ *   - "Mathematical Prerequisites for DeepSeek-V2" 6 (bilinear identity) and
+ *     7 (linearity): why the absorbed order gives the same result.
+ *
+ * Conventions for every call
+ *   - Every tensor pointer is DEVICE memory owned by the caller; the library
+ *     never allocates, frees or keeps a pointer after the call returns.
+ *   - Tensors are dense, row-major, in the layouts written beside each
+ *     argument.  Element type is dims->dtype (bf16 or fp32) unless stated.
+ *     Pointers must be 16-byte aligned; the cache pointer 128-byte aligned.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream).  No call synchronises except mla_get_error.
+ *   - Argument errors are detected on the host before anything is launched;
+ *     the call then returns MLA_ERR_INVALID_ARG or MLA_ERR_UNSUPPORTED and
+ *     leaves every buffer untouched.  A failed launch returns MLA_ERR_CUDA.
+ *   - Errors found on the device (a block-table entry outside [0,num_blocks),
+ *     a sequence length above max_seqlen or the table's capacity, a bounded
+ *     wait that expired) are recorded in the decode workspace's error word;
+ *     the affected rows are written as o_lat = 0, lse = -inf.  Read the word
+ *     with mla_get_error.
+ *   - Positions start at 0.  seqlens[b] counts tokens AFTER the current Hq
+ *     tokens were appended.  Query slot i (0 <= i < Hq) of sequence b sits
+ *     at position seqlens[b]-Hq+i and sees positions 0..seqlens[b]-Hq+i
+ *     (causal between slots).  A row that sees no position gets o_lat = 0
+ *     and lse = -inf.
+ */
+#ifndef MLA_H_
+#define MLA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same handle as cudaStream_t. */
+typedef struct CUstream_st *mla_stream_t;
+
+typedef enum {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad size            */
+  MLA_ERR_UNSUPPORTED = 2,   /* dims or dtype outside what the library runs */
+  MLA_ERR_WORKSPACE = 3,     /* workspace missing or too small              */
+  MLA_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed        */
+  MLA_ERR_DEVICE_BOUNDS = 5, /* device: block index / length out of range   */
+  MLA_ERR_TIMEOUT = 6        /* device: a bounded wait gave up              */
+} mla_status;
+
+typedef enum { MLA_BF16 = 0, MLA_FP32 = 1 } mla_dtype;
+
+/* Model dimensions.  H heads of width d_h; latent width d_c; decoupled RoPE
+ * width d_r (the cache row is d_c + d_r wide); block_size cache rows per
+ * physical block.  scale <= 0 selects 1/sqrt(d_h + d_r) ("MLA, dim by dim"
+ * 5.2).  Supported: 1 <= H <= 256, 1 <= d_h <= 128, 1 <= d_c <= 512,
+ * 0 <= d_r <= 64, 1 <= block_size <= 1024; both dtypes.  The tensor-core
+ * paths run bf16 with d_h = 128, d_c = 512, d_r = 64, block_size = 64; every
+ * other supported shape runs on CUDA-core kernels. */
+typedef struct {
+  int H, d_h, d_c, d_r, block_size;
+  mla_dtype dtype;
+  float scale;
+} mla_dims;
+
+/* Absorb W_UK into the query: q_lat[b,i,h,:] = W_UK[h]^T q_nope[b,i,h,:].
+ * ("From Vanilla Transformers to Modern LLMs -- Part 3" 3.e.2;
+ *  "MLA, dim by dim" 5.2, the bracketed left factor of the cached-decode score.)
+ *   q_nope [B, Hq, H, d_h]   input
+ *   W_UK   [H, d_h, d_c]     input, row-major per head (d_h rows of d_c)
+ *   q_lat  [B, Hq, H, d_c]   output (fp32 accumulation, rounded to dtype)
+ * B >= 0, Hq >= 1.  B == 0 is a no-op. */
+mla_status mla_absorb_query(const void *q_nope, const void *W_UK, void *q_lat,
+                            int B, int Hq, const mla_dims *dims,
+                            mla_stream_t stream);
+
+/* Append the n_new newest tokens of every sequence to the paged cache.
+ * Token i (0 <= i < n_new) of sequence b goes to position
+ * p = seqlens[b] - n_new + i: physical block block_table[b*max_blocks +
+ * p/block_size], row p % block_size, as [c_kv[b,i,:] ; k_r[b,i,:]].
+ * ("MLA Explained", decode step 5; "From Vanilla Transformers to Modern
+ *  LLMs -- Part 3" 3.q: k_R is stored already rotated.)
+ *   cache       [num_blocks, block_size, d_c + d_r]  in/out
+ *   block_table [B, max_blocks] int32                input
+ *   seqlens     [B] int32, lengths after the append  input
+ *   c_kv        [B, n_new, d_c]                      input
+ *   k_r         [B, n_new, d_r] (pre-rotated)        input (may be NULL iff d_r == 0)
+ * Positions p < 0 and block entries outside [0, num_blocks) are skipped
+ * (mla_decode reports the latter when it reads them). */
+mla_status mla_append_cache(void *cache, int num_blocks,
+                            const int32_t *block_table, int max_blocks,
+                            const int32_t *seqlens, const void *c_kv,
+                            const void *k_r, int B, int n_new,
+                            const mla_dims *dims, mla_stream_t stream);
+
+/* Bytes of device workspace mla_decode needs for this problem size.  The
+ * workspace holds the split-KV partials, the split plan and the error word.
+ * It must be zero-filled once before its first use; after that it may be
+ * reused by consecutive calls on one stream.  max_seqlen is an upper bound
+ * on seqlens[]. */
+mla_status mla_decode_workspace_size(int B, int Hq, int max_seqlen,
+                                     const mla_dims *dims, size_t *bytes);
+
+/* Absorbed MLA decode over the paged latent cache, split across the SMs
+ * along the sequence and merged by a log-sum-exp combine.
+ * For every b, query slot i, head h, with n = seqlens[b] - Hq + i + 1:
+ *   s_j   = (q_lat[b,i,h,:] . c_j + q_rope[b,i,h,:] . kR_j) * scale, j < n
+ *   p_j   = softmax_j(s_j)
+ *   o_lat[b,i,h,:] = sum_j p_j c_j          ("MLA, dim by dim" 4.2, 5.2)
+ *   lse[b,i,h]     = ln sum_j exp(s_j)      (natural log, scaled units)
+ * where row j of the sequence is cache[block_table[b][j/bs]][j%bs] =
+ * [c_j (d_c) ; kR_j (d_r)].
+ *   q_lat       [B, Hq, H, d_c]                    input
+ *   q_rope      [B, Hq, H, d_r] (pre-rotated)      input (NULL iff d_r == 0)
+ *   cache       [num_blocks, block_size, d_c+d_r]  input
+ *   block_table [B, max_blocks] int32              input
+ *   seqlens     [B] int32                          input
+ *   o_lat       [B, Hq, H, d_c]                    output (dtype)
+ *   lse         [B, Hq, H] float32                 output
+ *   workspace   >= mla_decode_workspace_size bytes, 256-byte aligned
+ * Consecutive calls that share a workspace must be ordered on one stream. */
+mla_status mla_decode(const void *q_lat, const void *q_rope, const void *cache,
+                      int num_blocks, const int32_t *block_table,
+                      int max_blocks, const int32_t *seqlens, int max_seqlen,
+                      int B, int Hq, const mla_dims *dims, void *o_lat,
+                      float *lse, void *workspace, size_t workspace_bytes,
+                      mla_stream_t stream);
+
+/* Expand the latent output through W_UV: out[b,i,h,:] = W_UV[h] o_lat[b,i,h,:].
+ * ("From Vanilla Transformers to Modern LLMs -- Part 3" 3.g; "MLA, dim by
+ *  dim" 4.2, the value chain contracted left to right.)
+ *   o_lat [B, Hq, H, d_c]   input
+ *   W_UV  [H, d_h, d_c]     input
+ *   out   [B, Hq, H, d_h]   output (fp32 accumulation, rounded to dtype) */
+mla_status mla_out_proj(const void *o_lat, const void *W_UV, void *out, int B,
+                        int Hq, const mla_dims *dims, mla_stream_t stream);
+
+/* Synchronise `stream`, read and clear the workspace's device error word.
+ * Returns MLA_OK, MLA_ERR_DEVICE_BOUNDS, MLA_ERR_TIMEOUT or MLA_ERR_CUDA. */
+mla_status mla_get_error(void *workspace, mla_stream_t stream);
+
+/* Static, human-readable name of a status code. */
+const char *mla_status_string(mla_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_H_ */

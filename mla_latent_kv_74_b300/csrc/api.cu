@@ -1,0 +1,153 @@
+// C-ABI entry points: host-side validation, path selection and launches.
+// Every entry point checks its arguments before launching anything; the
+// device kernels never allocate and never synchronise.
+#include <math.h>
+
+#include "internal.cuh"
+#include "tc.cuh"
+
+#define MLA_API extern "C" __attribute__((visibility("default")))
+
+namespace mla {
+namespace {
+
+bool dims_ok(const mla_dims *d) {
+  if (!d) return false;
+  if (d->dtype != MLA_BF16 && d->dtype != MLA_FP32) return false;
+  return d->H >= 1 && d->H <= kMaxH && d->d_h >= 1 && d->d_h <= kMaxDh && d->d_c >= 1 &&
+         d->d_c <= kMaxDc && d->d_r >= 0 && d->d_r <= kMaxDr && d->block_size >= 1 &&
+         d->block_size <= 1024 && isfinite(d->scale);
+}
+
+bool al(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+float eff_scale(const mla_dims *d) {
+  return d->scale > 0.f ? d->scale : 1.0f / sqrtf((float)(d->d_h + d->d_r));
+}
+
+mla_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA; }
+
+}  // namespace
+}  // namespace mla
+
+using namespace mla;
+
+MLA_API const char *mla_status_string(mla_status s) {
+  switch (s) {
+    case MLA_OK: return "MLA_OK";
+    case MLA_ERR_INVALID_ARG: return "MLA_ERR_INVALID_ARG: bad pointer, alignment or size";
+    case MLA_ERR_UNSUPPORTED: return "MLA_ERR_UNSUPPORTED: dims or dtype not supported";
+    case MLA_ERR_WORKSPACE: return "MLA_ERR_WORKSPACE: workspace missing or too small";
+    case MLA_ERR_CUDA: return "MLA_ERR_CUDA: a CUDA call or kernel launch failed";
+    case MLA_ERR_DEVICE_BOUNDS: return "MLA_ERR_DEVICE_BOUNDS: block index or length out of range";
+    case MLA_ERR_TIMEOUT: return "MLA_ERR_TIMEOUT: a bounded device wait gave up";
+  }
+  return "unknown mla_status";
+}
+
+MLA_API mla_status mla_absorb_query(const void *q_nope, const void *W_UK, void *q_lat, int B,
+                                    int Hq, const mla_dims *dims, mla_stream_t stream) {
+  if (!dims_ok(dims)) return dims ? MLA_ERR_UNSUPPORTED : MLA_ERR_INVALID_ARG;
+  if (B < 0 || Hq < 1) return MLA_ERR_INVALID_ARG;
+  if (B == 0) return MLA_OK;
+  if (!q_nope || !W_UK || !q_lat || !al(q_nope, 16) || !al(W_UK, 16) || !al(q_lat, 16))
+    return MLA_ERR_INVALID_ARG;
+  const int rows = B * Hq;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (tc_gemm_supported(*dims))
+    return cuda_status(launch_absorb_tc(q_nope, W_UK, q_lat, rows, *dims, st));
+  return cuda_status(launch_absorb_simt(q_nope, W_UK, q_lat, rows, *dims, st));
+}
+
+MLA_API mla_status mla_out_proj(const void *o_lat, const void *W_UV, void *out, int B, int Hq,
+                                const mla_dims *dims, mla_stream_t stream) {
+  if (!dims_ok(dims)) return dims ? MLA_ERR_UNSUPPORTED : MLA_ERR_INVALID_ARG;
+  if (B < 0 || Hq < 1) return MLA_ERR_INVALID_ARG;
+  if (B == 0) return MLA_OK;
+  if (!o_lat || !W_UV || !out || !al(o_lat, 16) || !al(W_UV, 16) || !al(out, 16))
+    return MLA_ERR_INVALID_ARG;
+  const int rows = B * Hq;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (tc_gemm_supported(*dims))
+    return cuda_status(launch_out_proj_tc(o_lat, W_UV, out, rows, *dims, st));
+  return cuda_status(launch_out_proj_simt(o_lat, W_UV, out, rows, *dims, st));
+}
+
+MLA_API mla_status mla_append_cache(void *cache, int num_blocks, const int32_t *block_table,
+                                    int max_blocks, const int32_t *seqlens, const void *c_kv,
+                                    const void *k_r, int B, int n_new, const mla_dims *dims,
+                                    mla_stream_t stream) {
+  if (!dims_ok(dims)) return dims ? MLA_ERR_UNSUPPORTED : MLA_ERR_INVALID_ARG;
+  if (B < 0 || n_new < 0 || num_blocks < 1 || max_blocks < 1) return MLA_ERR_INVALID_ARG;
+  if (B == 0 || n_new == 0) return MLA_OK;
+  if (!cache || !block_table || !seqlens || !c_kv || (dims->d_r > 0 && !k_r))
+    return MLA_ERR_INVALID_ARG;
+  if (!al(cache, 16) || !al(block_table, 4) || !al(seqlens, 4) || !al(c_kv, 16) ||
+      (k_r && !al(k_r, 16)))
+    return MLA_ERR_INVALID_ARG;
+  return cuda_status(launch_append(cache, num_blocks, block_table, max_blocks, seqlens, c_kv,
+                                   k_r, B, n_new, *dims,
+                                   reinterpret_cast<cudaStream_t>(stream)));
+}
+
+MLA_API mla_status mla_decode_workspace_size(int B, int Hq, int max_seqlen, const mla_dims *dims,
+                                             size_t *bytes) {
+  if (!bytes) return MLA_ERR_INVALID_ARG;
+  if (!dims_ok(dims)) return dims ? MLA_ERR_UNSUPPORTED : MLA_ERR_INVALID_ARG;
+  if (B < 0 || Hq < 1 || max_seqlen < 0) return MLA_ERR_INVALID_ARG;
+  size_t s = simt_workspace_bytes(B, Hq, max_seqlen, *dims);
+  if (tc_decode_supported(*dims)) {
+    const size_t t = tc_decode_workspace_bytes(B, Hq, *dims);
+    if (t > s) s = t;
+  }
+  *bytes = s;
+  return MLA_OK;
+}
+
+MLA_API mla_status mla_decode(const void *q_lat, const void *q_rope, const void *cache,
+                              int num_blocks, const int32_t *block_table, int max_blocks,
+                              const int32_t *seqlens, int max_seqlen, int B, int Hq,
+                              const mla_dims *dims, void *o_lat, float *lse, void *workspace,
+                              size_t workspace_bytes, mla_stream_t stream) {
+  if (!dims_ok(dims)) return dims ? MLA_ERR_UNSUPPORTED : MLA_ERR_INVALID_ARG;
+  if (B < 0 || Hq < 1 || max_seqlen < 0 || num_blocks < 1 || max_blocks < 1)
+    return MLA_ERR_INVALID_ARG;
+  if (B == 0) return MLA_OK;
+  if (!q_lat || !cache || !block_table || !seqlens || !o_lat || !lse ||
+      (dims->d_r > 0 && !q_rope))
+    return MLA_ERR_INVALID_ARG;
+  if (!al(q_lat, 16) || (q_rope && !al(q_rope, 16)) || !al(cache, 128) || !al(o_lat, 16) ||
+      !al(lse, 4) || !al(block_table, 4) || !al(seqlens, 4))
+    return MLA_ERR_INVALID_ARG;
+  if (!workspace || !al(workspace, 256)) return MLA_ERR_WORKSPACE;
+  size_t need = 0;
+  mla_decode_workspace_size(B, Hq, max_seqlen, dims, &need);
+  if (workspace_bytes < need) return MLA_ERR_WORKSPACE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const float scale = eff_scale(dims);
+  if (tc_decode_supported(*dims))
+    return cuda_status(launch_decode_tc(q_lat, q_rope, cache, num_blocks, block_table,
+                                        max_blocks, seqlens, max_seqlen, B, Hq, *dims, scale,
+                                        o_lat, lse, workspace, st));
+  return cuda_status(launch_decode_simt(q_lat, q_rope, cache, num_blocks, block_table,
+                                        max_blocks, seqlens, max_seqlen, B, Hq, *dims, scale,
+                                        o_lat, lse, workspace, st));
+}
+
+MLA_API mla_status mla_get_error(void *workspace, mla_stream_t stream) {
+  if (!workspace || !al(workspace, 256)) return MLA_ERR_WORKSPACE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int word = 0;
+  if (cudaMemcpyAsync(&word, workspace, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MLA_ERR_CUDA;
+  if (word != kDevOk) {
+    if (cudaMemsetAsync(workspace, 0, sizeof(int), st) != cudaSuccess) return MLA_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return MLA_ERR_CUDA;
+  }
+  const int gemm_word = read_and_clear_gemm_error();
+  if (gemm_word < 0) return MLA_ERR_CUDA;
+  if (word == kDevBounds) return MLA_ERR_DEVICE_BOUNDS;
+  if (word == kDevTimeout || gemm_word == kDevTimeout) return MLA_ERR_TIMEOUT;
+  return MLA_OK;
+}

@@ -1,0 +1,240 @@
+// Per-head batched GEMMs of the decode step on the 5th-generation tensor
+// cores (TMA -> shared memory -> tcgen05.mma -> TMEM -> registers -> global).
+//
+//   absorb   ("From Vanilla Transformers to Modern LLMs -- Part 3" 3.e.2):
+//     q_lat[r,h,c] = sum_a W_UK[h,a,c] q_nope[r,h,a]
+//     computed transposed, D[c][r] = A[c][a] B[r][a]: M = c (128 per CTA),
+//     N = query rows r, K = d_h.  A = W_UK[h] read MN-major (c contiguous).
+//   out_proj ("From Vanilla Transformers to Modern LLMs -- Part 3" 3.g):
+//     out[r,h,a] = sum_c W_UV[h,a,c] o_lat[r,h,c]
+//     D[a][r] = A[a][c] B[r][c]: M = a (d_h = 128), N = r, K = d_c.
+//     Both operands K-major.
+//
+// The weights are the large operand (16.8 MB per matrix at H = 128) and are
+// read exactly once; query rows (N <= 256 per CTA) are the small one.  One
+// CTA per (128-wide M tile, head, N tile); 4 warps: warp 0 issues TMA, warp 1
+// issues MMAs, warp 2 owns the TMEM allocation, all 4 drain the accumulator
+// (warp w reads TMEM lanes 32w..32w+31).  K is streamed in 64-wide chunks
+// through a ring of shared-memory stages (full / empty mbarriers).
+#include "internal.cuh"
+#include "ptx.cuh"
+#include "tc.cuh"
+#include "tmap.cuh"
+
+namespace mla {
+namespace {
+
+__device__ int g_gemm_error = 0;
+
+constexpr int kM = 128;
+constexpr int kKChunk = 64;  // one 128-byte swizzle span of bf16
+constexpr int kMaxStages = 4;
+constexpr uint32_t kABytes = kM * kKChunk * 2;  // 16 KB per chunk
+
+struct GemmArgs {
+  int num_k_chunks;  // K / 64
+  int rows;          // N extent (query rows)
+  int Nt;            // N per CTA (multiple of 16, <= 256)
+  int H;
+  int M_total;      // output width per head: d_c (absorb) or d_h (out_proj)
+  int a_rows_per_head;  // rows of the 2-D weight view per head (d_h)
+  int b_cols_per_head;  // columns of the 2-D activation view per head (K)
+  int stages;
+  __nv_bfloat16 *out;
+};
+
+template <bool kAMnMajor>
+__global__ void __launch_bounds__(128, 1)
+    head_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                     const __grid_constant__ CUtensorMap tmB, GemmArgs g) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // 1024-byte alignment of every operand tile (128B swizzle atoms).
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t b_bytes = g.Nt * 128;
+  const uint32_t stage_bytes = kABytes + b_bytes;
+  __shared__ uint64_t full[kMaxStages], empty[kMaxStages], done;
+  __shared__ uint32_t tmem_base;
+  __shared__ int fail;
+
+  const int warp = threadIdx.x >> 5;
+  const int m0 = blockIdx.x * kM;
+  const int h = blockIdx.y;
+  const int n0 = blockIdx.z * g.Nt;
+  const uint32_t ncols = g.Nt <= 32 ? 32 : (g.Nt <= 64 ? 64 : (g.Nt <= 128 ? 128 : 256));
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < g.stages; ++s) {
+      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&empty[s], 1);
+    }
+    ptx::mbar_init(&done, 1);
+    ptx::fence_mbar_init();
+    fail = 0;
+    ptx::tma_prefetch_desc(&tmA);
+    ptx::tma_prefetch_desc(&tmB);
+  }
+  if (warp == 2) ptx::tmem_alloc(&tmem_base, ncols);
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = tmem_base;
+
+  if (warp == 0 && ptx::elect_lane0()) {
+    // ---- TMA producer ----
+    int issued = 0;
+    for (int k = 0; k < g.num_k_chunks; ++k) {
+      const int s = k % g.stages;
+      if (k >= g.stages && !ptx::mbar_wait(&empty[s], ((k / g.stages) - 1) & 1, &fail)) {
+        atomicExch(&fail, 1);
+        break;
+      }
+      uint8_t *a_dst = smem + s * stage_bytes;
+      uint8_t *b_dst = a_dst + kABytes;
+      ptx::mbar_arrive_expect_tx(&full[s], stage_bytes);
+      if (kAMnMajor) {
+        // two 64(M) x 64(K) boxes: M block j at +8 KB
+        ptx::tma_load_2d(a_dst, &tmA, &full[s], m0, h * g.a_rows_per_head + k * kKChunk);
+        ptx::tma_load_2d(a_dst + 8192, &tmA, &full[s], m0 + 64,
+                         h * g.a_rows_per_head + k * kKChunk);
+      } else {
+        ptx::tma_load_2d(a_dst, &tmA, &full[s], k * kKChunk, h * g.a_rows_per_head + m0);
+      }
+      ptx::tma_load_2d(b_dst, &tmB, &full[s], h * g.b_cols_per_head + k * kKChunk, n0);
+      ++issued;
+    }
+    // never leave with copies in flight
+    for (int k = issued - g.stages < 0 ? 0 : issued - g.stages; k < issued; ++k)
+      if (!ptx::mbar_wait(&full[k % g.stages], (k / g.stages) & 1)) atomicExch(&fail, 1);
+  } else if (warp == 1 && ptx::elect_lane0()) {
+    // ---- MMA issuer ----
+    const uint32_t idesc = ptx::idesc_bf16(kM, g.Nt, kAMnMajor, false);
+    for (int k = 0; k < g.num_k_chunks; ++k) {
+      const int s = k % g.stages;
+      if (!ptx::mbar_wait(&full[s], (k / g.stages) & 1, &fail)) {
+        atomicExch(&fail, 1);
+        break;
+      }
+      ptx::tc_fence_after();
+      const uint32_t a_addr = ptx::smem_u32(smem + s * stage_bytes);
+      const uint32_t b_addr = a_addr + kABytes;
+#pragma unroll
+      for (int kk = 0; kk < kKChunk / 16; ++kk) {
+        const uint64_t adesc =
+            kAMnMajor ? ptx::smem_desc(a_addr + kk * 2048, 8192, 1024, ptx::kSw128)
+                      : ptx::smem_desc(a_addr + kk * 32, 16, 1024, ptx::kSw128);
+        const uint64_t bdesc = ptx::smem_desc(b_addr + kk * 32, 16, 1024, ptx::kSw128);
+        ptx::mma_bf16(tmem, adesc, bdesc, idesc, (k | kk) != 0);
+      }
+      ptx::mma_commit(&empty[s]);
+    }
+    ptx::mma_commit(&done);
+  }
+  __syncwarp();
+
+  // ---- epilogue: TMEM -> bf16 global, all 4 warps ----
+  const bool ok = ptx::mbar_wait(&done, 0);
+  ptx::tc_fence_after();
+  if (!ok) atomicExch(&fail, 1);
+  if (ok) {
+    const int m_local = warp * 32 + (threadIdx.x & 31);
+    const size_t row_stride = (size_t)g.H * g.M_total;
+    __nv_bfloat16 *dst = g.out + (size_t)h * g.M_total + m0 + m_local;
+    for (int c0 = 0; c0 < g.Nt; c0 += 16) {
+      float v[16];
+      ptx::tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + c0, v);
+      ptx::tmem_ld_wait();
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int n = n0 + c0 + i;
+        if (n < g.rows) dst[(size_t)n * row_stride] = __float2bfloat16_rn(v[i]);
+      }
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 2) ptx::tmem_dealloc(tmem, ncols);
+  if (threadIdx.x == 0 && fail) atomicCAS(&g_gemm_error, 0, kDevTimeout);
+}
+
+int pick_nt(int rows) {
+  const int r16 = (rows + 15) / 16 * 16;
+  return r16 > 256 ? 256 : r16;
+}
+
+template <bool kAMnMajor>
+cudaError_t launch_head_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, GemmArgs g,
+                             int m_tiles, cudaStream_t st) {
+  g.stages = g.num_k_chunks < kMaxStages ? g.num_k_chunks : kMaxStages;
+  const size_t smem = 1024 + (size_t)g.stages * (kABytes + g.Nt * 128);
+  auto kern = head_gemm_kernel<kAMnMajor>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(m_tiles, g.H, (g.rows + g.Nt - 1) / g.Nt);
+  kern<<<grid, 128, smem, st>>>(tmA, tmB, g);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool tc_gemm_supported(const mla_dims &d) {
+  return d.dtype == MLA_BF16 && d.d_h == 128 && d.d_c == 512;
+}
+
+int read_and_clear_gemm_error() {
+  int v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_gemm_error, sizeof(int)) != cudaSuccess) return -1;
+  if (v != 0) cudaMemcpyToSymbol(g_gemm_error, &zero, sizeof(int));
+  return v;
+}
+
+cudaError_t launch_absorb_tc(const void *q_nope, const void *W_UK, void *q_lat, int rows,
+                             const mla_dims &d, cudaStream_t st) {
+  CUtensorMap tmA, tmB;
+  const int Nt = pick_nt(rows);
+  // W_UK as [H*d_h rows][d_c cols]; boxes of 64 c x 64 a.
+  if (!make_tmap_2d_bf16(&tmA, W_UK, d.d_c, (uint64_t)d.H * d.d_h, (uint64_t)d.d_c * 2, 64, 64,
+                         CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  // q_nope as [rows][H*d_h]; boxes of 64 a x Nt rows.
+  if (!make_tmap_2d_bf16(&tmB, q_nope, (uint64_t)d.H * d.d_h, rows, (uint64_t)d.H * d.d_h * 2,
+                         64, Nt, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  GemmArgs g;
+  g.num_k_chunks = d.d_h / kKChunk;
+  g.rows = rows;
+  g.Nt = Nt;
+  g.H = d.H;
+  g.M_total = d.d_c;
+  g.a_rows_per_head = d.d_h;
+  g.b_cols_per_head = d.d_h;
+  g.out = static_cast<__nv_bfloat16 *>(q_lat);
+  return launch_head_gemm<true>(tmA, tmB, g, d.d_c / kM, st);
+}
+
+cudaError_t launch_out_proj_tc(const void *o_lat, const void *W_UV, void *out, int rows,
+                               const mla_dims &d, cudaStream_t st) {
+  CUtensorMap tmA, tmB;
+  const int Nt = pick_nt(rows);
+  // W_UV as [H*d_h rows][d_c cols]; boxes of 64 c x 128 a.
+  if (!make_tmap_2d_bf16(&tmA, W_UV, d.d_c, (uint64_t)d.H * d.d_h, (uint64_t)d.d_c * 2, 64, 128,
+                         CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  // o_lat as [rows][H*d_c]; boxes of 64 c x Nt rows.
+  if (!make_tmap_2d_bf16(&tmB, o_lat, (uint64_t)d.H * d.d_c, rows, (uint64_t)d.H * d.d_c * 2,
+                         64, Nt, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  GemmArgs g;
+  g.num_k_chunks = d.d_c / kKChunk;
+  g.rows = rows;
+  g.Nt = Nt;
+  g.H = d.H;
+  g.M_total = d.d_h;
+  g.a_rows_per_head = d.d_h;
+  g.b_cols_per_head = d.d_c;
+  g.out = static_cast<__nv_bfloat16 *>(out);
+  return launch_head_gemm<false>(tmA, tmB, g, 1, st);
+}
+
+}  // namespace mla

@@ -1,0 +1,28 @@
+// Tensor-core (tcgen05 / TMA) paths: shape predicates and launchers.
+#pragma once
+
+#include "internal.cuh"
+
+namespace mla {
+
+// bf16, d_h = 128, d_c = 512 (per-head GEMMs on tcgen05).
+bool tc_gemm_supported(const mla_dims &d);
+// bf16, d_c = 512, d_r = 64, block_size = 64 (paged TMA decode on tcgen05).
+bool tc_decode_supported(const mla_dims &d);
+size_t tc_decode_workspace_bytes(int B, int Hq, const mla_dims &d);
+
+cudaError_t launch_absorb_tc(const void *q_nope, const void *W_UK, void *q_lat, int rows,
+                             const mla_dims &d, cudaStream_t st);
+cudaError_t launch_out_proj_tc(const void *o_lat, const void *W_UV, void *out, int rows,
+                               const mla_dims &d, cudaStream_t st);
+cudaError_t launch_decode_tc(const void *q_lat, const void *q_rope, const void *cache,
+                             int num_blocks, const int32_t *block_table, int max_blocks,
+                             const int32_t *seqlens, int max_seqlen, int B, int Hq,
+                             const mla_dims &d, float scale, void *o_lat, float *lse,
+                             void *workspace, cudaStream_t st);
+
+// Read and clear the error word of the GEMM kernels (they take no workspace);
+// returns the device error code, or -1 if it could not be read.
+int read_and_clear_gemm_error();
+
+}  // namespace mla

@@ -204,16 +204,16 @@ def default_scale(d_h: int, d_r: int) -> float:
 
 
 def mla_decode(q_nope, q_rope, cache, block_table, seqlens, W_UK, W_UV, Hq,
-               scale=None, batch_indices=None):
+               scale=None, batch_indices=None, head_indices=None):
     """The whole decode step for the selected sequences.
 
     Shapes: ``q_nope [B, Hq, H, d_h]``, ``q_rope [B, Hq, H, d_r]``, ``cache
     [num_blocks, bs, d_c + d_r]``, ``block_table [B, max_blocks]``,
     ``seqlens [B]``, ``W_UK, W_UV [H, d_h, d_c]``.
 
-    Returns ``out [nb, Hq, H, d_h]``, ``o_lat [nb, Hq, H, d_c]`` and
-    ``lse [nb, Hq, H]`` for the ``nb`` sequences in ``batch_indices``
-    (all of them by default), in that order.
+    Returns ``out [nb, Hq, nh, d_h]``, ``o_lat [nb, Hq, nh, d_c]`` and
+    ``lse [nb, Hq, nh]`` for the ``nb`` sequences in ``batch_indices`` and the
+    ``nh`` heads in ``head_indices`` (all of them by default), in that order.
     """
     q_nope = np.asarray(q_nope, np.float64)
     q_rope = np.asarray(q_rope, np.float64)
@@ -226,13 +226,15 @@ def mla_decode(q_nope, q_rope, cache, block_table, seqlens, W_UK, W_UV, Hq,
     if batch_indices is None:
         batch_indices = range(B)
     batch_indices = list(batch_indices)
-    out = np.zeros((len(batch_indices), Hq, H, d_h))
-    o_lat = np.zeros((len(batch_indices), Hq, H, d_c))
-    lse = np.full((len(batch_indices), Hq, H), -math.inf)
+    head_indices = list(range(H)) if head_indices is None else list(head_indices)
+    nh = len(head_indices)
+    out = np.zeros((len(batch_indices), Hq, nh, d_h))
+    o_lat = np.zeros((len(batch_indices), Hq, nh, d_c))
+    lse = np.full((len(batch_indices), Hq, nh), -math.inf)
     for ob, b in enumerate(batch_indices):
         n_max = visible_length(seqlens[b], Hq, Hq - 1)
         all_rows = gather_sequence(cache, block_table[b], n_max)
-        for h in range(H):
+        for oh, h in enumerate(head_indices):
             # K_j and V_j of every visible position, rebuilt once per head and
             # shared by the query slots (slot i sees a prefix of them).
             K = reconstruct_keys(W_UK[h], all_rows[:, :d_c])
@@ -241,9 +243,9 @@ def mla_decode(q_nope, q_rope, cache, block_table, seqlens, W_UK, W_UV, Hq,
                 n = visible_length(seqlens[b], Hq, i)
                 r = attention_row(q_nope[b, i, h], q_rope[b, i, h], all_rows[:n],
                                   W_UK[h], W_UV[h], scale, d_c, K=K, V=V)
-                out[ob, i, h] = r["out"]
-                o_lat[ob, i, h] = r["o_lat"]
-                lse[ob, i, h] = r["lse"]
+                out[ob, i, oh] = r["out"]
+                o_lat[ob, i, oh] = r["o_lat"]
+                lse[ob, i, oh] = r["lse"]
     return out, o_lat, lse
 
 

@@ -1,0 +1,119 @@
+"""The C-ABI library loads, exports every symbol ``include/mla.h`` declares,
+and rejects bad arguments on the host before launching anything.
+
+These tests make no compute call: every call here fails validation and
+returns before touching CUDA, so they run on a machine without a GPU.
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import mla_latent_kv_74_b300 as m
+from mla_latent_kv_74_b300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_symbols():
+    txt = open(os.path.join(ROOT, "include", "mla.h")).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    return sorted(set(re.findall(r"\b(mla_[a-z_]+)\s*\(", txt)))
+
+
+def test_library_builds_and_loads():
+    path = build.build()
+    assert os.path.exists(path)
+    ctypes.CDLL(path)
+
+
+def test_every_declared_symbol_is_exported():
+    declared = _declared_symbols()
+    assert set(declared) == set(m.EXPORTED), declared
+    lib = ctypes.CDLL(m.LIB_PATH)
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_status_strings():
+    for code in range(7):
+        s = m.status_string(code)
+        assert s.startswith("MLA_")
+    assert m.status_string(99) == "unknown mla_status"
+
+
+def _dims(**kw):
+    base = dict(H=128, d_h=128, d_c=512, d_r=64, block_size=64, dtype=m.MLA_BF16)
+    base.update(kw)
+    return m.Dims(**base)
+
+
+def test_workspace_size_validation():
+    lib = m.raw_lib()
+    n = ctypes.c_size_t()
+    assert lib.mla_decode_workspace_size(4, 1, 100, None, ctypes.byref(n)) == m.MLA_ERR_INVALID_ARG
+    assert lib.mla_decode_workspace_size(4, 1, 100, ctypes.byref(_dims(d_c=1024)),
+                                         ctypes.byref(n)) == m.MLA_ERR_UNSUPPORTED
+    assert lib.mla_decode_workspace_size(4, 0, 100, ctypes.byref(_dims()),
+                                         ctypes.byref(n)) == m.MLA_ERR_INVALID_ARG
+    assert lib.mla_decode_workspace_size(4, 1, 100, ctypes.byref(_dims()), None) == \
+        m.MLA_ERR_INVALID_ARG
+    assert lib.mla_decode_workspace_size(64, 1, 8192, ctypes.byref(_dims()),
+                                         ctypes.byref(n)) == m.MLA_OK
+    assert n.value >= 256
+
+
+@pytest.mark.parametrize("bad", [dict(H=0), dict(H=300), dict(d_h=256), dict(d_r=65),
+                                 dict(block_size=0), dict(dtype=7)])
+def test_unsupported_dims_rejected(bad):
+    lib = m.raw_lib()
+    d = _dims(**bad)
+    p = ctypes.c_void_p(256)
+    assert lib.mla_absorb_query(p, p, p, 1, 1, ctypes.byref(d), None) == m.MLA_ERR_UNSUPPORTED
+    assert lib.mla_out_proj(p, p, p, 1, 1, ctypes.byref(d), None) == m.MLA_ERR_UNSUPPORTED
+
+
+def test_null_and_misaligned_pointers_rejected():
+    lib = m.raw_lib()
+    d = ctypes.byref(_dims())
+    ok = ctypes.c_void_p(1 << 20)
+    mis = ctypes.c_void_p((1 << 20) + 2)
+    assert lib.mla_absorb_query(None, ok, ok, 1, 1, d, None) == m.MLA_ERR_INVALID_ARG
+    assert lib.mla_absorb_query(ok, mis, ok, 1, 1, d, None) == m.MLA_ERR_INVALID_ARG
+    assert lib.mla_out_proj(ok, ok, mis, 1, 1, d, None) == m.MLA_ERR_INVALID_ARG
+    assert lib.mla_append_cache(ok, 4, ok, 4, ok, ok, None, 1, 1, d, None) == \
+        m.MLA_ERR_INVALID_ARG  # k_r missing with d_r > 0
+    # decode: cache must be 128-byte aligned, workspace present and large enough
+    cache_mis = ctypes.c_void_p((1 << 20) + 64)
+    args = [ok, ok, cache_mis, 4, ok, 4, ok, 64, 1, 1, d, ok, ok, ok, 1 << 30, None]
+    assert lib.mla_decode(*args) == m.MLA_ERR_INVALID_ARG
+    args[2] = ok
+    args[13] = None
+    assert lib.mla_decode(*args) == m.MLA_ERR_WORKSPACE
+    args[13] = ok
+    args[14] = 16
+    assert lib.mla_decode(*args) == m.MLA_ERR_WORKSPACE
+    args[9] = 0  # Hq
+    assert lib.mla_decode(*args) == m.MLA_ERR_INVALID_ARG
+
+
+def test_empty_batch_is_a_noop():
+    lib = m.raw_lib()
+    d = ctypes.byref(_dims())
+    assert lib.mla_absorb_query(None, None, None, 0, 1, d, None) == m.MLA_OK
+    assert lib.mla_out_proj(None, None, None, 0, 1, d, None) == m.MLA_OK
+    assert lib.mla_append_cache(None, 1, None, 1, None, None, None, 0, 1, d, None) == m.MLA_OK
+    assert lib.mla_decode(None, None, None, 1, None, 1, None, 0, 0, 1, d, None, None, None, 0,
+                          None) == m.MLA_OK
+
+
+def test_strided_tensor_refused():
+    """A strided view would be read as dense memory: the binding refuses it."""
+    import torch
+    t = torch.zeros(4, 8).t()
+    with pytest.raises(ValueError):
+        m._ptr(t)
+    x = torch.zeros(4, 8)
+    assert m._ptr(x) == x.data_ptr()
