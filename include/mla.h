@@ -164,6 +164,42 @@ mla_status mla_get_error(void *workspace, mla_stream_t stream);
 /* Static, human-readable name of a status code. */
 const char *mla_status_string(mla_status status);
 
+/* Bytes of the scratch array built into the library for mla_decode_noalloc.
+ * Every GPU that loads the library holds this much device memory until the
+ * process exits. */
+#define MLA_NOALLOC_SCRATCH_BYTES ((size_t)48 << 20)
+
+/* mla_decode for callers that cannot allocate device memory.
+ * The paper has no counterpart to this call: it exists for deployment only.
+ * mla_decode needs a workspace that the caller allocates; some callers cannot
+ * call cudaMalloc (a plugin inside a host application that owns all device
+ * memory and exposes no allocator, or a serving loop that must never block on
+ * an allocation).  This variant takes the workspace from a fixed array of
+ * MLA_NOALLOC_SCRATCH_BYTES compiled into the library and allocates nothing:
+ * no cudaMalloc, no cudaFree, no allocating library routine.
+ *   Arguments, layouts and results are those of mla_decode, minus the
+ *   workspace.  The caller still provides every input and output.
+ *   - A problem whose workspace (mla_decode_workspace_size) exceeds
+ *     MLA_NOALLOC_SCRATCH_BYTES is rejected with MLA_ERR_WORKSPACE before
+ *     anything is launched.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before any stream capture.
+ *   - All calls share the one array, which keeps the last call's contents;
+ *     each call clears the part that must start at zero (the error word)
+ *     before its kernels run.  Calls that overlap on the GPU (different
+ *     streams, or different host threads without ordering) race on the array
+ *     and give undefined results: order them on one stream.
+ *   - Device-side errors are not reported through mla_get_error (the
+ *     workspace is private); the affected rows still come back as o_lat = 0,
+ *     lse = -inf. */
+mla_status mla_decode_noalloc(const void *q_lat, const void *q_rope,
+                              const void *cache, int num_blocks,
+                              const int32_t *block_table, int max_blocks,
+                              const int32_t *seqlens, int max_seqlen, int B,
+                              int Hq, const mla_dims *dims, void *o_lat,
+                              float *lse, mla_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

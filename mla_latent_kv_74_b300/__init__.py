@@ -5,7 +5,7 @@ marshal arguments: tensors become raw device pointers, the stream becomes a
 ``cudaStream_t``, and a non-``MLA_OK`` status raises :class:`MLAError`.
 Every step of the path runs in the library's CUDA kernels; there is no CPU
 or PyTorch fallback.  Importing this package fails loudly when the library
-has not been built (``python -m mla_latent_kv_74_b300.build``).
+has not been built (``python mla_latent_kv_74_b300/build.py``).
 
 Example (one decode step, all tensors on ``cuda``)::
 
@@ -48,7 +48,11 @@ EXPORTED = (
     "mla_out_proj",
     "mla_get_error",
     "mla_status_string",
+    "mla_decode_noalloc",
 )
+
+# size of the scratch array built into the library for mla_decode_noalloc
+NOALLOC_SCRATCH_BYTES = 48 << 20
 
 
 class MLAError(RuntimeError):
@@ -77,7 +81,7 @@ class Dims(ctypes.Structure):
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(
-            f"{LIB_PATH} is missing: build it with `python -m mla_latent_kv_74_b300.build`")
+            f"{LIB_PATH} is missing: build it with `python mla_latent_kv_74_b300/build.py`")
     lib = ctypes.CDLL(LIB_PATH)
     P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
     D = ctypes.POINTER(Dims)
@@ -89,6 +93,7 @@ def _load():
         "mla_out_proj": [P, P, P, I, I, D, P],
         "mla_get_error": [P, P],
         "mla_status_string": [I],
+        "mla_decode_noalloc": [P, P, P, I, P, I, P, I, I, I, D, P, P, P],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -176,6 +181,18 @@ def mla_out_proj(o_lat, W_UV, out, dims: Dims, stream=None):
     B, Hq = o_lat.shape[0], o_lat.shape[1]
     _check(_lib.mla_out_proj(_ptr(o_lat), _ptr(W_UV), _ptr(out), B, Hq, ctypes.byref(dims),
                              _stream(stream)), "mla_out_proj")
+
+
+def mla_decode_noalloc(q_lat, q_rope, cache, num_blocks, block_table, seqlens, max_seqlen,
+                       dims: Dims, o_lat, lse, stream=None):
+    """``mla_decode`` without a caller-provided workspace: the library uses
+    its built-in scratch array (for callers that cannot allocate device
+    memory).  Calls share that array, so order them on one stream."""
+    B, Hq = q_lat.shape[0], q_lat.shape[1]
+    _check(_lib.mla_decode_noalloc(_ptr(q_lat), _ptr(q_rope), _ptr(cache), int(num_blocks),
+                                   _ptr(block_table), block_table.shape[1], _ptr(seqlens),
+                                   int(max_seqlen), B, Hq, ctypes.byref(dims), _ptr(o_lat),
+                                   _ptr(lse), _stream(stream)), "mla_decode_noalloc")
 
 
 def mla_get_error(workspace, stream=None) -> int:

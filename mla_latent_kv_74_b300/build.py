@@ -1,8 +1,10 @@
 """Build ``libmla.so`` (the C-ABI library) in-tree with nvcc for sm_103a.
 
-    python -m mla_latent_kv_74_b300.build          # build if sources changed
-    python -m mla_latent_kv_74_b300.build --force  # always rebuild
-    python -m mla_latent_kv_74_b300.build --verbose-ptxas  # print -Xptxas -v
+    python mla_latent_kv_74_b300/build.py                  # build if sources changed
+    python mla_latent_kv_74_b300/build.py --force          # always rebuild
+    python mla_latent_kv_74_b300/build.py --verbose-ptxas  # print -Xptxas -v
+
+(Run it by path: the package's __init__ loads the library this script builds.)
 
 Each ``csrc/*.cu`` compiles to an object under ``_build/`` (in parallel) and
 the objects link into ``mla_latent_kv_74_b300/libmla.so``.  No GPU is needed:

@@ -8,6 +8,21 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 
+def _ensure_library_built():
+    """Build libmla.so (nvcc, no GPU needed) when it is missing or older than
+    its sources, before any test imports the binding."""
+    import importlib.util
+
+    path = os.path.join(ROOT, "mla_latent_kv_74_b300", "build.py")
+    spec = importlib.util.spec_from_file_location("_mla_build", path)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    mod.build()
+
+
+_ensure_library_built()
+
+
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (B300, sm_103a)")
     config.addinivalue_line("markers", "slow: long-running CPU test")

@@ -12,7 +12,6 @@ import re
 import pytest
 
 import mla_latent_kv_74_b300 as m
-from mla_latent_kv_74_b300 import build
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
@@ -24,9 +23,8 @@ def _declared_symbols():
 
 
 def test_library_builds_and_loads():
-    path = build.build()
-    assert os.path.exists(path)
-    ctypes.CDLL(path)
+    assert os.path.exists(m.LIB_PATH)
+    ctypes.CDLL(m.LIB_PATH)
 
 
 def test_every_declared_symbol_is_exported():
