@@ -12,22 +12,30 @@
 // latent accumulator O (128 heads x 512) or the full query, not both:
 //   * the S-CTA (cluster rank 1) keeps the item's query [q_lat ; q_rope]
 //     (128 x 576 bf16 = 288 columns) in TMEM as the A operand of
-//     S = Q C^T (M=128, N=64, K=576, three S buffers in the other 192
-//     columns), runs the online softmax and ships P (bf16) to its peer;
+//     S = Q C^T (M=128, N=64, K=576; three S buffers in the other columns),
+//     runs the online softmax and ships P (bf16) to its peer;
 //   * the V-CTA (rank 0) keeps O (512 columns) in TMEM and accumulates
-//     O += P C (M=128, N=2x256, K=64) from P in its shared memory.
-// Every cache tile is loaded once from HBM: each CTA issues half of the
-// latent boxes with TMA multicast to both CTAs (the S-CTA also loads the
-// RoPE box for itself), so the two CTAs see the same 64 x 512 latent tile at
-// the same shared-memory offset.  A stage is refilled only when both the
-// QK^T of the S-CTA and the PV of the V-CTA that read it have completed
-// (tcgen05.commit multicast to both CTAs' "empty" barriers).
+//     O += P C (M=128, N=2x256, K=64) with P in its shared memory.
+// Each CTA streams the cache through its own ring of shared-memory stages:
+// the S-CTA loads [c_KV ; k_R] tiles (HBM) and frees a stage as soon as its
+// QK^T is done; the V-CTA loads the latent part of the same tiles a little
+// later (L2 hits) and frees a stage after its PV.  Decoupling the rings keeps
+// the long HBM latency off the softmax -> PV chain.  Two warps of the S-CTA
+// issue QK^T for alternate tiles, so two accumulation chains keep the tensor
+// pipe busy at N = 64.
 //
-// Messages from the S-CTA to the V-CTA travel by st.async into the V-CTA's
-// shared memory, each counted by an mbarrier: per tile the P tile (16 KB,
-// already in the 128B-swizzled K-major layout of the MMA), the per-row
-// rescale factor and four per-warp rescale flags; per segment the row
-// statistics (running max and sum) the epilogue needs.
+// P goes straight into the V-CTA's shared memory by st.async (distributed
+// shared memory, counted on the destination mbarrier), already in the
+// 128B-swizzled K-major layout of the MMA operand, with the rows' rescale
+// factors and four per-warp rescale flags; one P buffer per tile parity.
+// Two groups of four softmax warps take alternate tiles, so one group's
+// transfer overlaps the other's exponentials.  The groups agree on the
+// running maximum through shared memory (a tile's maximum is published
+// before its exponentials, so the next tile waits only for that), keep
+// their own row sums, and merge them at each segment end before the row
+// statistics go to the V-CTA (st.async).  The V-CTA's correction warps apply
+// the rare O rescales and run each segment's epilogue, staging O through the
+// last tile's P buffer and writing it with TMA stores.
 //
 // Online softmax in base 2 with lazy rescaling: the running maximum moves
 // (and O is rescaled by the V-CTA's correction warps) only when a tile's
@@ -40,9 +48,10 @@
 // combine_tc_kernel merges with log-sum-exp weights; whole items are written
 // directly.  The plan is computed on the device from seqlens (no host sync).
 //
-// Warp roles (192 threads per CTA): warp 0 TMA producer, warp 1 TMEM owner
-// and MMA issuer, warps 2-5 softmax (S-CTA) or rescale / epilogue (V-CTA);
-// warp w of 2-5 owns TMEM lanes (rows) 32*(w%4) .. 32*(w%4)+31.
+// Warp roles (352 threads per CTA): warp 0 TMA producer, warp 1 TMEM owner
+// and MMA issuer; S-CTA: warp 6 second QK^T issuer, warps 2-5 and 7-10 the
+// two softmax groups (even / odd tiles); V-CTA: warps 2-5 rescale and
+// epilogue.  A warp w that touches TMEM owns lanes 32*(w%4) .. 32*(w%4)+31.
 //
 // Every wait is bounded; a lost wait records MLA_ERR_TIMEOUT in the
 // workspace, tells the peer CTA to stop, and the CTA unwinds (no trap).
@@ -60,49 +69,64 @@ constexpr int kMaxPairs = kNumSMs / 2;  // 74 clusters of 2 CTAs
 constexpr int kTile = 64;               // tokens per tile = block size
 constexpr int kDc = 512, kDr = 64, kD = kDc + kDr;
 constexpr int kStages = 3;
-constexpr int kMaxItems = 1024;  // B * Hq limit of this path
-constexpr int kPrefetchTiles = 6;  // L2 prefetch distance (tiles)
+constexpr int kThreads = 352;
+constexpr int kMaxItems = 1024;    // B * Hq limit of this path
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2(256)
 
 constexpr uint32_t kRankV = 0, kRankS = 1;
-constexpr uint16_t kMaskBoth = 0x3, kMaskS = 1u << kRankS;
+constexpr uint16_t kMaskS = 1u << kRankS;
 
-// ---- shared memory (offsets from the dynamic base, identical in both CTAs)
-constexpr uint32_t kBox = 64 * 128;                   // 64 rows x 128 B, 128B swizzle
-constexpr uint32_t kLatStage = 8 * kBox;              // 64 tokens x 512 latent
-constexpr uint32_t kOffLat = 0;                       // both: [kStages][8 boxes]
-constexpr uint32_t kOffRope = kStages * kLatStage;    // S: [kStages] RoPE boxes
-constexpr uint32_t kOffPrefix = kOffRope + kStages * kBox;  // S: tiles prefix [W+1]
-constexpr uint32_t kOffP = kStages * kLatStage;       // V: [2] P tiles
-constexpr uint32_t kPBytes = 128 * 128;               // 128 rows x 64 bf16
-constexpr uint32_t kOffAlpha = kOffP + 2 * kPBytes;   // V: [2][128] f32
-constexpr uint32_t kOffFlags = kOffAlpha + 2 * 128 * 4;  // V: [2][4] u32
-constexpr uint32_t kOffStats = kOffFlags + 2 * 16;    // V: m[128], l[128]
-constexpr uint32_t kOffBars = kOffStats + 2 * 128 * 4;
-constexpr uint32_t kMsgBytes = kPBytes + 128 * 4 + 16;  // one P message
+// ---- shared memory (offsets from the 1024-aligned dynamic base)
+constexpr uint32_t kBox = 64 * 128;                // 64 rows x 128 B, 128B swizzle
+constexpr uint32_t kOffRing = 0;
+// S-CTA: [kStages] x (8 latent boxes + 1 RoPE box), query staging, the
+// published running maximum, one group's row statistics at a segment end
+constexpr uint32_t kSStage = 9 * kBox;
+constexpr uint32_t kOffQStage = kStages * kSStage;  // 4 warps x 32 rows x 64 B
+constexpr uint32_t kQStageBytes = 4 * 2048;
+constexpr uint32_t kOffMDec = kOffQStage + kQStageBytes;  // m[128] f32
+constexpr uint32_t kOffLM = kOffMDec + 128 * 4;           // m[128], l[128] f32
+constexpr uint32_t kSEnd = kOffLM + 2 * 128 * 4;
+// V-CTA: [kStages] x 8 latent boxes, P buffer per tile parity, their rescale
+// factors and flags, row statistics
+constexpr uint32_t kVStage = 8 * kBox;
+constexpr uint32_t kOffP = kStages * kVStage;
+constexpr uint32_t kPBytes = 128 * 128;            // 128 rows x 64 bf16
+constexpr uint32_t kAuxBytes = 128 * 4 + 16;       // alpha[128] f32, flags[4] u32
+constexpr uint32_t kOffAux = kOffP + 2 * kPBytes;
+constexpr uint32_t kOffStats = kOffAux + 2 * kAuxBytes;  // m[128], l[128]
 constexpr uint32_t kStatsBytes = 2 * 128 * 4;
-static_assert(kOffPrefix + (kMaxItems + 1) * 4 <= kOffAlpha, "S-CTA prefix overlaps");
+constexpr uint32_t kVEnd = kOffStats + kStatsBytes;
+constexpr uint32_t kMsgBytes = kPBytes + kAuxBytes;  // one P message
+// both
+constexpr uint32_t kOffBars = kSEnd > kVEnd ? kSEnd : kVEnd;
+static_assert(kOffP % 1024 == 0, "P buffers must be 1024-byte aligned");
 
 struct Bars {
-  uint64_t full[kStages], empty[kStages];
-  uint64_t s_full[3], s_free[3];   // S: score buffers
-  uint64_t p_full[2];              // V: P messages arrived
-  uint64_t p_free[2];              // S: V-CTA done with a P buffer
-  uint64_t q_full, q_free;         // S: query in TMEM / QK^T of a segment done
-  uint64_t stats_full;             // V: row statistics arrived
-  uint64_t stats_free;             // S: V-CTA read the statistics
-  uint64_t o_full, pv_done;        // V: accumulator complete
-  uint64_t ev_full, ev_done;       // V: MMA warp <-> correction warps
-  uint64_t drain;
+  uint64_t full[kStages], empty[kStages];  // each CTA's own ring (V: full)
+  // S: per tile g, barrier g % 6 (stage g % 3, issuer and softmax group
+  // g % 2), so each barrier has one waiter that never falls a phase behind
+  uint64_t sfull[6];                       // S: tile data landed
+  uint64_t s_full[6], s_free[6];           // S: scores ready / read
+  uint64_t q_full, q_free;                 // S: query in TMEM / QK^T of a segment done
+  uint64_t m_ready[2];                     // S: group i published its tile's maximum
+  uint64_t seg_sync[2];                    // S: both softmax groups at a segment end
+  uint64_t p_free[2];                      // S: V-CTA done with P buffer i
+  uint64_t stats_free;                     // S: V-CTA read the statistics
+  uint64_t p_full[2];                      // V: P message i arrived
+  uint64_t stats_full;                     // V: row statistics arrived
+  uint64_t o_full, pv_done;                // V: accumulator complete
+  uint64_t ev_full, ev_done;               // V: MMA warp <-> correction warps
+  uint64_t drain[2];
 };
 
 struct Misc {
   uint32_t tmem;
   int abort;
-  int ev_type;  // kEvRescale | buffer << 4, kEvEpilogue, kEvDone
-  int per, t_begin, t_end, w0, t_total;
+  int ev_type;  // kEvRescale | buffer << 4, kEvEpilogue | buffer << 4, kEvDone
+  int t_begin, t_end, w0, s0, t_total;
   int bad_smem;
 };
 constexpr int kEvRescale = 1, kEvEpilogue = 2, kEvDone = 3;
@@ -129,7 +153,26 @@ struct DecodeArgs {
   float *lse_part;  // [2 * kMaxPairs][128]
   int *plan;        // [0] = tiles per pair, [1..W+1] = prefix of tiles per item
   int *err;
+  int tma_olat;     // o_lat rows can be written with 32-row TMA boxes (H % 32 == 0)
 };
+
+#ifdef MLA_TRACE
+// Developer tracing (built only with -DMLA_TRACE): %globaltimer stamps per
+// tile and role for two pairs (the first and the middle one), read back
+// with mla_debug_read_trace.  Events: 0 producer issued the tile's loads,
+// 1 MMA warp saw the tile's data, 2 S: QK^T issued / V: P arrived, 3 S:
+// softmax exponentials done / V: PV issued, 4 S: softmax saw S, 5 S: P buffer
+// free, 6 S: P sent, 7 per segment: S query loaded / V epilogue done.
+constexpr int kTraceTiles = 512, kTraceEvents = 8, kTracePairs = 2;
+__device__ unsigned long long g_trace[kTracePairs][2][kTraceEvents][kTraceTiles];
+__device__ __forceinline__ void trace_ev(int pair, int npairs, uint32_t rank, int ev, int g) {
+  const int slot = pair == 0 ? 0 : (pair == npairs / 2 ? 1 : -1);
+  if (slot >= 0 && g >= 0 && g < kTraceTiles) g_trace[slot][rank][ev][g] = ptx::globaltimer_ns();
+}
+#define MLA_TRACE_EV(ev, g) trace_ev(pair, a.npairs, rank, (ev), (g))
+#else
+#define MLA_TRACE_EV(ev, g) ((void)0)
+#endif
 
 __device__ __forceinline__ int visible_len(const DecodeArgs &a, int w, bool *bad) {
   const int b = w / a.Hq, slot = w % a.Hq;
@@ -140,6 +183,11 @@ __device__ __forceinline__ int visible_len(const DecodeArgs &a, int w, bool *bad
   }
   const int n = sl - a.Hq + slot + 1;
   return n > 0 ? n : 0;
+}
+
+__device__ __forceinline__ int item_tiles(const DecodeArgs &a, int w) {
+  bool bad = false;
+  return (visible_len(a, w, &bad) + kTile - 1) / kTile;
 }
 
 __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort) {
@@ -155,41 +203,36 @@ __device__ __forceinline__ bool wait_bar_warp(uint64_t *bar, uint32_t parity, vo
   return __all_sync(0xffffffffu, ok);
 }
 
-// Prefix of tiles per item, read from the S-CTA's shared memory (locally or
-// through distributed shared memory).
-struct Prefix {
-  const int *local;
-  uint32_t remote;
-  __device__ int operator()(int i) const {
-    return local ? local[i] : ptx::ld_cluster_s32(remote + 4u * (uint32_t)i);
-  }
-};
-
 // The segments of one pair: consecutive (item, tile range) pieces of its
-// range [t_begin, t_end) of the global tile order, starting at item w0.
+// range [t_begin, t_end) of the global tile order, walked from item w0
+// (whose first tile has global index s0); tile counts come from seqlens.
 struct SegIter {
-  Prefix pre;
-  int W, t_begin, t_end, w;
-  __device__ void init(Prefix p, int W_, int tb, int te, int w0) {
-    pre = p;
+  const DecodeArgs *a;
+  int W, t_begin, t_end, w, s;
+  __device__ void init(const DecodeArgs *args, int W_, int tb, int te, int w0, int s0) {
+    a = args;
     W = W_;
     t_begin = tb;
     t_end = te;
     w = w0;
+    s = s0;
   }
-  // next non-empty segment: item, first and end local tile; false when done
-  __device__ bool next(int *item, int *lt0, int *lt1, bool *whole) {
-    while (w < W) {
-      const int s = pre(w), e = pre(w + 1);
-      if (s >= t_end) return false;
+  // next non-empty segment: item, first and end local tile, visible length
+  __device__ bool next(int *item, int *lt0, int *lt1, bool *whole, int *n_vis) {
+    while (w < W && s < t_end) {
+      bool bad = false;
+      const int n = visible_len(*a, w, &bad);
+      const int st = s, e = s + (n + kTile - 1) / kTile;
       const int cur = w++;
-      if (e <= s || e <= t_begin) continue;
-      const int g0 = s > t_begin ? s : t_begin;
+      s = e;
+      if (e <= st || e <= t_begin) continue;
+      const int g0 = st > t_begin ? st : t_begin;
       const int g1 = e < t_end ? e : t_end;
       *item = cur;
-      *lt0 = g0 - s;
-      *lt1 = g1 - s;
-      *whole = (g0 == s) && (g1 == e);
+      *lt0 = g0 - st;
+      *lt1 = g1 - st;
+      *whole = (g0 == st) && (g1 == e);
+      *n_vis = n;
       return true;
     }
     return false;
@@ -223,8 +266,10 @@ __device__ __forceinline__ void signal_abort(Misc *misc, uint32_t peer) {
   ptx::st_cluster_s32(ptx::map_to_rank(&misc->abort, peer), 1);
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
-    decode_tc_kernel(const __grid_constant__ CUtensorMap tm_cache, DecodeArgs a) {
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    decode_tc_kernel(const __grid_constant__ CUtensorMap tm_cache,
+                     const __grid_constant__ CUtensorMap tm_olat,
+                     const __grid_constant__ CUtensorMap tm_opart, DecodeArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
   Bars *bars = reinterpret_cast<Bars *>(smem + kOffBars);
   Misc *misc = reinterpret_cast<Misc *>(smem + kOffMisc);
@@ -236,9 +281,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
   const int pair = blockIdx.x >> 1;
   const int W = a.B * a.Hq;
   volatile int *abort = &misc->abort;
-  int *s_prefix = reinterpret_cast<int *>(smem + kOffPrefix);
 
-  // ---- setup: barriers, TMEM, tile plan ----
+  // ---- setup: barriers, TMEM, this pair's tile range ----
   if (threadIdx.x == 0) {
     misc->abort = 0;
     misc->ev_type = 0;
@@ -246,42 +290,52 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     misc->bad_smem = (ptx::smem_u32(smem) & 1023u) != 0;
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(&bars->full[s], 1);
-      ptx::mbar_init(&bars->empty[s], 2);
+      ptx::mbar_init(&bars->empty[s], 1);
     }
-    for (int s = 0; s < 3; ++s) {
+    for (int s = 0; s < 6; ++s) {
+      ptx::mbar_init(&bars->sfull[s], 1);
       ptx::mbar_init(&bars->s_full[s], 1);
       ptx::mbar_init(&bars->s_free[s], 128);
     }
-    for (int s = 0; s < 2; ++s) {
-      ptx::mbar_init(&bars->p_full[s], 1);
-      ptx::mbar_init(&bars->p_free[s], 1);
-    }
     ptx::mbar_init(&bars->q_full, 128);
-    ptx::mbar_init(&bars->q_free, 1);
-    ptx::mbar_init(&bars->stats_full, 1);
+    ptx::mbar_init(&bars->q_free, 2);
+    for (int s = 0; s < 2; ++s) {
+      ptx::mbar_init(&bars->m_ready[s], 128);
+      ptx::mbar_init(&bars->seg_sync[s], 256);
+      ptx::mbar_init(&bars->p_free[s], 1);
+      ptx::mbar_init(&bars->p_full[s], 1);
+      ptx::mbar_init(&bars->drain[s], 1);
+    }
     ptx::mbar_init(&bars->stats_free, 4);
+    ptx::mbar_init(&bars->stats_full, 1);
     ptx::mbar_init(&bars->o_full, 1);
     ptx::mbar_init(&bars->pv_done, 1);
     ptx::mbar_init(&bars->ev_full, 1);
     ptx::mbar_init(&bars->ev_done, 128);
-    ptx::mbar_init(&bars->drain, 1);
     ptx::fence_mbar_init();
-    if (!isS) {  // arm the first message phases the S-CTA will fill
+    if (!isS) {  // the first message phases the S-CTA fills
       ptx::mbar_arrive_expect_tx(&bars->p_full[0], kMsgBytes);
       ptx::mbar_arrive_expect_tx(&bars->p_full[1], kMsgBytes);
       ptx::mbar_arrive_expect_tx(&bars->stats_full, kStatsBytes);
     }
   }
-  if (warp == 0 && lane == 0) ptx::tma_prefetch_desc(&tm_cache);
+  if (warp == 0 && lane == 0) {
+    ptx::tma_prefetch_desc(&tm_cache);
+    if (!isS) {
+      ptx::tma_prefetch_desc(&tm_olat);
+      ptx::tma_prefetch_desc(&tm_opart);
+    }
+  }
   if (warp == 1) ptx::tmem_alloc(&misc->tmem, 512);
   if (isS) {
-    // tiles per item -> s_prefix[w + 1], then an inclusive scan
+    // tiles per item -> scan (scratch in the ring) -> this pair's range
+    int *pre = reinterpret_cast<int *>(smem + kOffRing);
     bool any_bad = false;
     for (int w = threadIdx.x; w < W; w += blockDim.x) {
       bool bad = false;
       const int n = visible_len(a, w, &bad);
       any_bad |= bad;
-      s_prefix[w + 1] = (n + kTile - 1) / kTile;
+      pre[w + 1] = (n + kTile - 1) / kTile;
     }
     if (any_bad && pair == 0) set_device_error(a.err, kDevBounds);
     __syncthreads();
@@ -289,254 +343,243 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
       int running = 0;
       for (int base = 0; base < W; base += 32) {
         const int idx = base + lane;
-        int v = idx < W ? s_prefix[idx + 1] : 0;
+        int v = idx < W ? pre[idx + 1] : 0;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
           const int u = __shfl_up_sync(0xffffffffu, v, off);
           if (lane >= off) v += u;
         }
-        if (idx < W) s_prefix[idx + 1] = running + v;
+        if (idx < W) pre[idx + 1] = running + v;
         running += __shfl_sync(0xffffffffu, v, 31);
       }
-      if (lane == 0) s_prefix[0] = 0;
+      if (lane == 0) pre[0] = 0;
     }
     __syncthreads();
     if (threadIdx.x == 0) {
-      const int t_total = s_prefix[W];
+      const int t_total = pre[W];
       const int per = (t_total + a.npairs - 1) / a.npairs;
       const int tb = min(t_total, pair * per);
       const int te = min(t_total, tb + per);
-      // first item whose tile range ends after tb
-      int lo = 0, hi = W;
+      int lo = 0, hi = W;  // first item whose tile range ends after tb
       while (lo < hi) {
         const int mid = (lo + hi) >> 1;
-        if (s_prefix[mid + 1] <= tb) lo = mid + 1;
+        if (pre[mid + 1] <= tb) lo = mid + 1;
         else hi = mid;
       }
-      misc->per = per;
       misc->t_begin = tb;
       misc->t_end = te;
       misc->w0 = lo;
+      misc->s0 = lo < W ? pre[lo] : t_total;
       misc->t_total = t_total;
+      if (pair == 0) a.plan[0] = per;
     }
-    if (blockIdx.x == 1) {  // the S-CTA of pair 0 publishes the plan for the combine
-      if (threadIdx.x == 0) a.plan[0] = (s_prefix[W] + a.npairs - 1) / a.npairs;
-      for (int w = threadIdx.x; w <= W; w += blockDim.x) a.plan[1 + w] = s_prefix[w];
-    }
+    if (pair == 0)  // the plan of the combine kernel
+      for (int w = threadIdx.x; w <= W; w += blockDim.x) a.plan[1 + w] = pre[w];
+    __syncthreads();  // the scratch is the ring: read before the first load
   }
   ptx::tc_fence_before();
   __syncthreads();
-  ptx::cluster_sync();  // both CTAs started, barriers initialised, plan computed
+  ptx::cluster_sync();  // both CTAs started, barriers initialised, range computed
   ptx::tc_fence_after();
 
   const uint32_t tmem = misc->tmem;
   const bool bad_smem = misc->bad_smem != 0;
-  Prefix pre;
-  pre.local = isS ? s_prefix : nullptr;
-  pre.remote = isS ? 0u : ptx::map_to_rank(s_prefix, kRankS);
-  // this pair's tile range (the V-CTA reads the S-CTA's values)
-  int t_begin, t_end, w0;
+  int t_begin, t_end, w0, s0;
   if (isS) {
     t_begin = misc->t_begin;
     t_end = misc->t_end;
     w0 = misc->w0;
-  } else {
+    s0 = misc->s0;
+  } else {  // the V-CTA reads the S-CTA's values
     t_begin = ptx::ld_cluster_s32(ptx::map_to_rank(&misc->t_begin, kRankS));
     t_end = ptx::ld_cluster_s32(ptx::map_to_rank(&misc->t_end, kRankS));
     w0 = ptx::ld_cluster_s32(ptx::map_to_rank(&misc->w0, kRankS));
+    s0 = ptx::ld_cluster_s32(ptx::map_to_rank(&misc->s0, kRankS));
   }
 
   if (bad_smem) {
     if (threadIdx.x == 0) set_device_error(a.err, kDevTimeout);
   } else if (warp == 0) {
-    // ===================== TMA producer (both CTAs) =====================
+    // ===================== TMA producer (each CTA its own ring) =====================
     SegIter it;
-    it.init(pre, W, t_begin, t_end, w0);
-    int item, lt0, lt1, g = 0;
-    bool whole;
-    TableWindow cur, ahead;
-    const uint32_t tx_bytes = isS ? kLatStage + kBox : kLatStage;
-    const int box0 = isS ? 4 : 0;
-    while (!*abort && it.next(&item, &lt0, &lt1, &whole)) {
+    it.init(&a, W, t_begin, t_end, w0, s0);
+    int item, lt0, lt1, n_vis, g = 0;
+    bool whole, failed = false;
+    TableWindow cur;
+    const uint32_t stage_bytes = isS ? kSStage : kVStage;
+    const int nbox = isS ? 9 : 8;
+    while (!failed && !*abort && it.next(&item, &lt0, &lt1, &whole, &n_vis)) {
       const int b = item / a.Hq;
-      const int32_t *tbl = a.block_table + (size_t)b * a.max_blocks;
-      cur.reset(tbl, lt1);
-      ahead.reset(tbl, lt1);
+      cur.reset(a.block_table + (size_t)b * a.max_blocks, lt1);
       if (isS && lane == 0) {  // the query the softmax warps load next
         const size_t row0 = (size_t)item * a.H;
         const int nrows = a.H < 128 ? a.H : 128;
         ptx::prefetch_l2(a.q_lat + row0 * kDc, (uint32_t)nrows * kDc * 2);
         ptx::prefetch_l2(a.q_rope + row0 * kDr, (uint32_t)nrows * kDr * 2);
       }
-      bool failed = false;
       for (int lt = lt0; lt < lt1; ++lt, ++g) {
         const int st = g % kStages;
-        if (g >= kStages &&
-            !wait_bar_warp(&bars->empty[st], ((g / kStages) - 1) & 1, abort)) {
+        if (g >= kStages && !wait_bar_warp(&bars->empty[st], ((g / kStages) - 1) & 1, abort)) {
           failed = true;
           break;
         }
         int blk = cur.at(lt, lane);
         if (blk < 0 || blk >= a.num_blocks) blk = 0;  // reported by the softmax warps
         if (lane == 0) {
-          uint8_t *dst = smem + kOffLat + st * kLatStage;
-          ptx::mbar_arrive_expect_tx(&bars->full[st], tx_bytes);
-          for (int k = 0; k < 4; ++k)
-            ptx::tma_load_2d_mc(dst + (box0 + k) * kBox, &tm_cache, &bars->full[st],
-                                (box0 + k) * 64, blk * kTile, kMaskBoth);
-          if (isS)
-            ptx::tma_load_2d(smem + kOffRope + st * kBox, &tm_cache, &bars->full[st], kDc,
-                             blk * kTile);
+          MLA_TRACE_EV(0, g);
+          uint8_t *dst = smem + kOffRing + st * stage_bytes;
+          uint64_t *fb = isS ? &bars->sfull[g % 6] : &bars->full[st];
+          ptx::mbar_arrive_expect_tx(fb, nbox * kBox);
+          for (int k = 0; k < nbox; ++k)
+            ptx::tma_load_2d(dst + k * kBox, &tm_cache, fb, k * 64, blk * kTile);
         }
-        const int lp = lt + kPrefetchTiles;
-        if (lp < lt1) {
-          int pblk = ahead.at(lp, lane);
-          if (lane == 0 && pblk >= 0 && pblk < a.num_blocks) {
-            for (int k = 0; k < 4; ++k) ptx::tma_prefetch_2d(&tm_cache, (box0 + k) * 64, pblk * kTile);
-            if (isS) ptx::tma_prefetch_2d(&tm_cache, kDc, pblk * kTile);
-          }
-        }
-      }
-      if (failed) {
-        signal_abort(misc, peer);
-        break;
       }
     }
-    // Leave only when both CTAs are done with every stage this CTA filled:
-    // all loads have landed and no multicast commit is still on its way.
+    if (failed) signal_abort(misc, peer);
+    // leave only after this CTA's consumers released every stage it filled
     if (!*abort)
       for (int k = g - kStages < 0 ? 0 : g - kStages; k < g; ++k)
         wait_bar_warp(&bars->empty[k % kStages], (k / kStages) & 1, abort);
-  } else if (warp == 1) {
-    if (isS) {
-      // ===================== S-CTA: QK^T issuer =====================
-      if (lane == 0) {
-        const uint32_t idesc = ptx::idesc_bf16(128, kTile, false, false);
-        const uint32_t lat_addr = ptx::smem_u32(smem + kOffLat);
-        const uint32_t rope_addr = ptx::smem_u32(smem + kOffRope);
-        SegIter it;
-        it.init(pre, W, t_begin, t_end, w0);
-        int item, lt0, lt1, seg = 0, g = 0;
-        bool whole, failed = false;
-        while (!failed && it.next(&item, &lt0, &lt1, &whole)) {
-          if (!wait_bar(&bars->q_full, seg & 1, abort)) { failed = true; break; }
+  } else if (isS && (warp == 1 || warp == 6)) {
+    // ========== S-CTA: QK^T issuers (warp 1 even tiles, warp 6 odd tiles) ==========
+    if (lane == 0) {
+      const int mine = warp == 1 ? 0 : 1;
+      const uint32_t idesc = ptx::idesc_bf16(128, kTile, false, false);
+      const uint64_t ring_desc = ptx::smem_desc(ptx::smem_u32(smem + kOffRing), 16, 1024, ptx::kSw128);
+      SegIter it;
+      it.init(&a, W, t_begin, t_end, w0, s0);
+      int item, lt0, lt1, n_vis, seg = 0, g = 0;
+      bool whole, failed = false;
+      while (!failed && it.next(&item, &lt0, &lt1, &whole, &n_vis)) {
+        if (!wait_bar(&bars->q_full, seg & 1, abort)) { failed = true; break; }
+        ptx::tc_fence_after();
+        for (int lt = lt0; lt < lt1; ++lt, ++g) {
+          if ((g & 1) != mine) continue;
+          const int st = g % kStages, sb = g % 3;
+          if (!wait_bar(&bars->sfull[g % 6], (g / 6) & 1, abort)) { failed = true; break; }
+          MLA_TRACE_EV(1, g);
+          // score buffer sb was last read by the softmax of tile g-3
+          if (g >= 3 && !wait_bar(&bars->s_free[(g - 3) % 6], ((g - 3) / 6) & 1, abort)) { failed = true; break; }
           ptx::tc_fence_after();
-          for (int lt = lt0; lt < lt1; ++lt, ++g) {
-            const int st = g % kStages, sb = g % 3;
-            if (!wait_bar(&bars->full[st], (g / kStages) & 1, abort)) { failed = true; break; }
-            if (g >= 3 && !wait_bar(&bars->s_free[sb], ((g / 3) - 1) & 1, abort)) { failed = true; break; }
-            ptx::tc_fence_after();
-            const uint32_t d = tmem + kTmemS + sb * kTile;
-            const uint32_t lat = lat_addr + st * kLatStage;
+          const uint32_t d = tmem + kTmemS + sb * kTile;
+          const uint64_t bs = ring_desc + (uint64_t)((st * kSStage) >> 4);
 #pragma unroll
-            for (int kk = 0; kk < 32; ++kk) {  // latent: 8 boxes x 4 k-steps of 16
-              const uint64_t bd =
-                  ptx::smem_desc(lat + (kk >> 2) * kBox + (kk & 3) * 32, 16, 1024, ptx::kSw128);
-              ptx::mma_bf16_ts(d, tmem + kTmemQ + kk * 8, bd, idesc, kk != 0);
-            }
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {  // RoPE: one box, 4 k-steps
-              const uint64_t bd =
-                  ptx::smem_desc(rope_addr + st * kBox + kk * 32, 16, 1024, ptx::kSw128);
-              ptx::mma_bf16_ts(d, tmem + kTmemQ + 256 + kk * 8, bd, idesc, 1u);
-            }
-            ptx::mma_commit(&bars->s_full[sb]);
-            ptx::mma_commit_mc(&bars->empty[st], kMaskBoth);
-          }
-          if (failed) break;
-          ptx::mma_commit(&bars->q_free);
-          ++seg;
+          for (int kk = 0; kk < 36; ++kk)  // 9 boxes (8 latent + RoPE) x 4 k-steps of 16
+            ptx::mma_bf16_ts(d, tmem + kTmemQ + kk * 8,
+                             bs + (uint64_t)((((kk >> 2) * kBox) + (kk & 3) * 32) >> 4), idesc,
+                             kk != 0);
+          ptx::mma_commit(&bars->s_full[g % 6]);
+          ptx::mma_commit(&bars->empty[st]);
+          MLA_TRACE_EV(2, g);
         }
-        ptx::mma_commit(&bars->drain);
-        ptx::mbar_wait(&bars->drain, 0);
-        if (failed) signal_abort(misc, peer);
+        if (failed) break;
+        ptx::mma_commit(&bars->q_free);
+        ++seg;
       }
-    } else {
-      // ===================== V-CTA: PV issuer =====================
-      if (lane == 0) {
-        const uint32_t idesc = ptx::idesc_bf16(128, 256, false, true);
-        const uint32_t lat_addr = ptx::smem_u32(smem + kOffLat);
-        const uint32_t p_addr = ptx::smem_u32(smem + kOffP);
-        const uint32_t *flags = reinterpret_cast<const uint32_t *>(smem + kOffFlags);
-        SegIter it;
-        it.init(pre, W, t_begin, t_end, w0);
-        int item, lt0, lt1, seg = 0, g = 0, nev = 0, npv = 0;
-        bool whole, failed = false;
-        auto post = [&](int type) -> bool {
-          misc->ev_type = type;
-          ptx::mbar_arrive(&bars->ev_full);
-          const bool ok = wait_bar(&bars->ev_done, nev & 1, abort);
-          ++nev;
-          return ok;
-        };
-        while (!failed && it.next(&item, &lt0, &lt1, &whole)) {
-          for (int lt = lt0; lt < lt1; ++lt, ++g) {
-            const int st = g % kStages, pb = g & 1;
-            if (!wait_bar(&bars->full[st], (g / kStages) & 1, abort)) { failed = true; break; }
-            if (!wait_bar_cl(&bars->p_full[pb], (g >> 1) & 1, abort)) { failed = true; break; }
-            const volatile uint32_t *f = flags + 4 * pb;
-            const bool resc = lt != lt0 && ((f[0] | f[1] | f[2] | f[3]) != 0);
-            if (resc) {
-              // O *= alpha (per row) once the previous PV has accumulated
-              ptx::mma_commit(&bars->pv_done);
-              if (!wait_bar(&bars->pv_done, npv & 1, abort)) { failed = true; break; }
-              ++npv;
-              if (!post(kEvRescale | (pb << 4))) { failed = true; break; }
-            }
-            // the next message into this buffer comes after the PV below
-            ptx::mbar_arrive_expect_tx(&bars->p_full[pb], kMsgBytes);
-            ptx::fence_proxy_async_smem();  // P was written by st.async
-            ptx::tc_fence_after();
-            const uint32_t lat = lat_addr + st * kLatStage;
-#pragma unroll
-            for (int kk = 0; kk < kTile / 16; ++kk) {
-              const uint64_t ad =
-                  ptx::smem_desc(p_addr + pb * kPBytes + kk * 32, 16, 1024, ptx::kSw128);
-#pragma unroll
-              for (int h = 0; h < 2; ++h) {
-                const uint64_t bd =
-                    ptx::smem_desc(lat + h * 4 * kBox + kk * 2048, 4 * 2048, 1024, ptx::kSw128);
-                ptx::mma_bf16(tmem + kTmemO + h * 256, ad, bd, idesc,
-                              (lt == lt0 && kk == 0) ? 0u : 1u);
-              }
-            }
-            ptx::mma_commit_mc(&bars->p_free[pb], kMaskS);
-            ptx::mma_commit_mc(&bars->empty[st], kMaskBoth);
-          }
-          if (failed) break;
-          ptx::mma_commit(&bars->o_full);
-          if (!wait_bar(&bars->o_full, seg & 1, abort)) { failed = true; break; }
-          if (!post(kEvEpilogue)) { failed = true; break; }
-          ++seg;
-        }
-        misc->ev_type = kEvDone;
-        ptx::mbar_arrive(&bars->ev_full);
-        ptx::mma_commit(&bars->drain);
-        ptx::mbar_wait(&bars->drain, 0);
-        if (failed) signal_abort(misc, peer);
-      }
+      uint64_t *dr = &bars->drain[mine];
+      ptx::mma_commit(dr);
+      ptx::mbar_wait(dr, 0);
+      if (failed) signal_abort(misc, peer);
     }
-  } else if (isS) {
-    // ===================== S-CTA: softmax (warps 2-5) =====================
-    const int row = 32 * (warp & 3) + lane;
-    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-    SegIter it;
-    it.init(pre, W, t_begin, t_end, w0);
-    int item, lt0, lt1, seg = 0, g = 0;
-    bool whole, failed = false;
-    // remote (V-CTA) addresses of the message buffers and their barriers
-    const uint32_t rP = ptx::map_to_rank(smem + kOffP, kRankV);
-    const uint32_t rAlpha = ptx::map_to_rank(smem + kOffAlpha, kRankV);
-    const uint32_t rFlags = ptx::map_to_rank(smem + kOffFlags, kRankV);
+  } else if (!isS && warp == 1) {
+    // ===================== V-CTA: PV issuer =====================
+    if (lane == 0) {
+      const uint32_t idesc = ptx::idesc_bf16(128, 256, false, true);
+      const uint64_t p_desc = ptx::smem_desc(ptx::smem_u32(smem + kOffP), 16, 1024, ptx::kSw128);
+      const uint64_t ring_desc =
+          ptx::smem_desc(ptx::smem_u32(smem + kOffRing), 4 * 2048, 1024, ptx::kSw128);
+      const uint8_t *aux = smem + kOffAux;
+      SegIter it;
+      it.init(&a, W, t_begin, t_end, w0, s0);
+      int item, lt0, lt1, n_vis, seg = 0, g = 0, nev = 0, npv = 0;
+      bool whole, failed = false;
+      auto post = [&](int type) -> bool {
+        misc->ev_type = type;
+        ptx::mbar_arrive(&bars->ev_full);
+        const bool ok = wait_bar(&bars->ev_done, nev & 1, abort);
+        ++nev;
+        return ok;
+      };
+      while (!failed && it.next(&item, &lt0, &lt1, &whole, &n_vis)) {
+        for (int lt = lt0; lt < lt1; ++lt, ++g) {
+          const int st = g % kStages, pb = g & 1;
+          if (!wait_bar(&bars->full[st], (g / kStages) & 1, abort)) { failed = true; break; }
+          MLA_TRACE_EV(1, g);
+          if (!wait_bar_cl(&bars->p_full[pb], (g >> 1) & 1, abort)) { failed = true; break; }
+          MLA_TRACE_EV(2, g);
+          const volatile uint32_t *fl =
+              reinterpret_cast<const volatile uint32_t *>(aux + pb * kAuxBytes + 512);
+          const uint32_t any = fl[0] | fl[1] | fl[2] | fl[3];
+          if (lt != lt0 && any != 0) {
+            // O *= alpha (per row) once every PV so far has accumulated
+            ptx::mma_commit(&bars->pv_done);
+            if (!wait_bar(&bars->pv_done, npv & 1, abort)) { failed = true; break; }
+            ++npv;
+            if (!post(kEvRescale | (pb << 4))) { failed = true; break; }
+          }
+          // the next message into this buffer comes after the PV below
+          ptx::mbar_arrive_expect_tx(&bars->p_full[pb], kMsgBytes);
+          ptx::fence_proxy_async_smem();  // P arrived by st.async (generic proxy)
+          ptx::tc_fence_after();
+          const uint64_t ad0 = p_desc + (uint64_t)((pb * kPBytes) >> 4);
+          const uint64_t bd0 = ring_desc + (uint64_t)((st * kVStage) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+              ptx::mma_bf16(tmem + kTmemO + h * 256, ad0 + (uint64_t)((kk * 32) >> 4),
+                            bd0 + (uint64_t)((h * 4 * kBox + kk * 2048) >> 4), idesc,
+                            (lt == lt0 && kk == 0) ? 0u : 1u);
+          }
+          ptx::mma_commit(&bars->empty[st]);
+          // the last tile's P buffer becomes the epilogue's staging
+          if (lt != lt1 - 1) ptx::mma_commit_mc(&bars->p_free[pb], kMaskS);
+          MLA_TRACE_EV(3, g);
+        }
+        if (failed) break;
+        ptx::mma_commit(&bars->o_full);
+        if (!wait_bar(&bars->o_full, seg & 1, abort)) { failed = true; break; }
+        const int last_pb = (g - 1) & 1;
+        if (!post(kEvEpilogue | (last_pb << 4))) { failed = true; break; }
+        ptx::mbar_arrive_remote(&bars->p_free[last_pb], kRankS);  // staging handed back
+        ++seg;
+      }
+      misc->ev_type = kEvDone;
+      ptx::mbar_arrive(&bars->ev_full);
+      ptx::mma_commit(&bars->drain[0]);
+      ptx::mbar_wait(&bars->drain[0], 0);
+      if (failed) signal_abort(misc, peer);
+    }
+  } else if (isS && ((warp >= 2 && warp <= 5) || (warp >= 7 && warp <= 10))) {
+    // ====== S-CTA: softmax, group 0 (warps 2-5) even tiles, group 1 (7-10) odd ======
+    const int grp = warp >= 7 ? 1 : 0;
+    const int wq = warp & 3;
+    const int row = 32 * wq + lane;
+    const uint32_t lane_base = (uint32_t)(32 * wq) << 16;
+    const int gtid = threadIdx.x - (grp ? 224 : 64);  // 0..127 within the group
+    uint8_t *qst = smem + kOffQStage + wq * 2048;     // 32 rows x 64 B
+    float *m_dec = reinterpret_cast<float *>(smem + kOffMDec);
+    float *lm = reinterpret_cast<float *>(smem + kOffLM);
+    const uint32_t rP = ptx::map_to_rank(smem + kOffP + grp * kPBytes, kRankV);
+    const uint32_t rAux = ptx::map_to_rank(smem + kOffAux + grp * kAuxBytes, kRankV);
+    const uint32_t rPFull = ptx::map_to_rank(&bars->p_full[grp], kRankV);
     const uint32_t rStats = ptx::map_to_rank(smem + kOffStats, kRankV);
-    const uint32_t rPFull0 = ptx::map_to_rank(&bars->p_full[0], kRankV);
-    const uint32_t rPFull1 = ptx::map_to_rank(&bars->p_full[1], kRankV);
     const uint32_t rStatsFull = ptx::map_to_rank(&bars->stats_full, kRankV);
     const float c = a.scale_log2;
-    while (!failed && it.next(&item, &lt0, &lt1, &whole)) {
-      bool dummy = false;
-      const int n_vis = visible_len(a, item, &dummy);
+    (void)gtid;
+    SegIter it;
+    it.init(&a, W, t_begin, t_end, w0, s0);
+    int item, lt0, lt1, n_vis, seg = 0, g = 0;
+    bool whole, failed = false;
+    // both softmax groups meet twice per segment end (bounded waits, one
+    // phase per segment on each barrier)
+    auto group_bar = [&](int which) -> bool {
+      ptx::mbar_arrive(&bars->seg_sync[which]);
+      return wait_bar_warp(&bars->seg_sync[which], seg & 1, abort);
+    };
+    while (!failed && it.next(&item, &lt0, &lt1, &whole, &n_vis)) {
       const int b = item / a.Hq;
+      const int g_first = g, g_last = g + (lt1 - lt0) - 1;
       // block-table entries this segment reads (each warp on its own)
       bool seg_bad;
       {
@@ -548,44 +591,77 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         }
         seg_bad = __any_sync(0xffffffffu, bad);
       }
-      // -- this item's query -> TMEM (row = lane), once the previous
-      //    segment's QK^T no longer reads it --
+      // -- this item's query -> TMEM (loaded by the group owning the first
+      //    tile), once the previous segment's QK^T no longer reads it --
       if (seg > 0 && !wait_bar_warp(&bars->q_free, (seg - 1) & 1, abort)) { failed = true; break; }
-      ptx::tc_fence_after();
-      {
-        const bool valid = row < a.H;
-        const size_t grow = (size_t)item * a.H + row;
-        const uint4 *ql = reinterpret_cast<const uint4 *>(a.q_lat + grow * kDc);
-        const uint4 *qr = reinterpret_cast<const uint4 *>(a.q_rope + grow * kDr);
+      if ((g_first & 1) == grp) {
+        ptx::tc_fence_after();
+        const size_t row0 = (size_t)item * a.H + 32 * wq;
+        const int nvalid = a.H - 32 * wq;  // rows of this warp that exist
+        // coalesced loads (4 lanes per 64-byte piece of a row), transposed
+        // through shared memory to one row per lane
+        auto load_chunk = [&](int chunk, uint4 (&v)[4]) {
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {  // 2 x 9 chunks of 16 columns
-          uint32_t v[9][16];
-#pragma unroll
-          for (int cc = 0; cc < 9; ++cc) {
-            const int chunk = half * 9 + cc;  // 0..15 latent, 16..17 RoPE
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              uint4 x = make_uint4(0, 0, 0, 0);
-              if (valid) x = chunk < 16 ? __ldg(ql + chunk * 4 + q) : __ldg(qr + (chunk - 16) * 4 + q);
-              v[cc][4 * q] = x.x;
-              v[cc][4 * q + 1] = x.y;
-              v[cc][4 * q + 2] = x.z;
-              v[cc][4 * q + 3] = x.w;
+          for (int i = 0; i < 4; ++i) {
+            const int r = 8 * i + (lane >> 2), part = lane & 3;
+            v[i] = make_uint4(0, 0, 0, 0);
+            if (r < nvalid) {
+              const uint4 *src = chunk < 16
+                  ? reinterpret_cast<const uint4 *>(a.q_lat + (row0 + r) * kDc + chunk * 32)
+                  : reinterpret_cast<const uint4 *>(a.q_rope + (row0 + r) * kDr + (chunk - 16) * 32);
+              v[i] = __ldg(src + part);
             }
           }
+        };
+        uint4 cur[3][4], nxt[3][4];
 #pragma unroll
-          for (int cc = 0; cc < 9; ++cc)
-            ptx::tmem_st16_nc(tmem + lane_base + kTmemQ + (half * 9 + cc) * 16, v[cc]);
+        for (int j = 0; j < 3; ++j) load_chunk(j, cur[j]);
+#pragma unroll
+        for (int gp = 0; gp < 6; ++gp) {
+          if (gp < 5) {
+#pragma unroll
+            for (int j = 0; j < 3; ++j) load_chunk(3 * (gp + 1) + j, nxt[j]);
+          }
+#pragma unroll
+          for (int j = 0; j < 3; ++j) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int r = 8 * i + (lane >> 2), part = lane & 3;
+              *reinterpret_cast<uint4 *>(qst + r * 64 + ((part ^ ((r >> 1) & 3)) << 4)) = cur[j][i];
+            }
+            __syncwarp();
+            uint32_t v[16];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint4 x = *reinterpret_cast<const uint4 *>(qst + lane * 64 + ((k ^ ((lane >> 1) & 3)) << 4));
+              v[4 * k] = x.x;
+              v[4 * k + 1] = x.y;
+              v[4 * k + 2] = x.z;
+              v[4 * k + 3] = x.w;
+            }
+            ptx::tmem_st16_nc(tmem + lane_base + kTmemQ + (3 * gp + j) * 16, v);
+            __syncwarp();
+          }
+          if (gp < 5) {
+#pragma unroll
+            for (int j = 0; j < 3; ++j)
+#pragma unroll
+              for (int i = 0; i < 4; ++i) cur[j][i] = nxt[j][i];
+          }
         }
         ptx::tmem_st_wait();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(&bars->q_full);
+        if (lane == 0 && wq == 0) MLA_TRACE_EV(7, seg);
       }
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(&bars->q_full);
 
-      float m_run = -INFINITY, l_run = 0.f;
+      // this group's row sum over its tiles of the segment, relative to m_mine
+      float m_mine = -INFINITY, l_mine = 0.f;
       for (int lt = lt0; lt < lt1; ++lt, ++g) {
-        const int sb = g % 3, pb = g & 1;
-        if (!wait_bar_warp(&bars->s_full[sb], (g / 3) & 1, abort)) { failed = true; break; }
+        if ((g & 1) != grp) continue;
+        const int sb = g % 3;
+        if (!wait_bar_warp(&bars->s_full[g % 6], (g / 6) & 1, abort)) { failed = true; break; }
+        if (lane == 0 && wq == 0) MLA_TRACE_EV(4, g);
         ptx::tc_fence_after();
         float s[64];
 #pragma unroll
@@ -597,7 +673,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         }
         ptx::tmem_ld_wait();
         ptx::tc_fence_before();
-        ptx::mbar_arrive(&bars->s_free[sb]);
+        ptx::mbar_arrive(&bars->s_free[g % 6]);
         const int tok0 = lt * kTile;
         if (tok0 + kTile > n_vis) {
 #pragma unroll
@@ -608,15 +684,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
 #pragma unroll
         for (int j = 1; j < 64; ++j) mx = fmaxf(mx, s[j]);
         const float mt = mx * c;
-        float m_use = m_run, alpha = 1.f;
+        // the previous tile's maximum (published by the other group)
+        if (g > 0 && !wait_bar_warp(&bars->m_ready[grp ^ 1], ((g - 1) >> 1) & 1, abort)) { failed = true; break; }
+        float m_use = mt, alpha = 1.f;
         bool resc = false;
-        if (lt == lt0) {
-          m_use = mt;
-        } else if (mt > m_run + kRescaleThreshold) {
-          m_use = mt;
-          alpha = ptx::ex2(m_run - mt);
-          resc = true;
+        if (lt != lt0) {
+          const float m_prev = m_dec[row];
+          if (mt > m_prev + kRescaleThreshold) {
+            alpha = ptx::ex2(m_prev - mt);
+            resc = true;
+          } else {
+            m_use = m_prev;
+          }
         }
+        m_dec[row] = m_use;
+        ptx::mbar_arrive(&bars->m_ready[grp]);
         uint32_t pk[32];
         float lsum = 0.f;
 #pragma unroll
@@ -626,29 +708,45 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
           lsum += p0 + p1;
           pk[i] = ptx::pack_bf16x2(p0, p1);
         }
-        l_run = l_run * alpha + lsum;
-        m_run = m_use;
-        // P buffer pb was last read by the V-CTA's PV of tile g-2
-        if (g >= 2 && !wait_bar_warp(&bars->p_free[pb], ((g >> 1) - 1) & 1, abort, true)) {
+        if (m_use != m_mine) {  // the maximum moved since this group's last tile
+          l_mine = (m_mine == -INFINITY) ? 0.f : l_mine * ptx::ex2(m_mine - m_use);
+          m_mine = m_use;
+        }
+        l_mine += lsum;
+        if (lane == 0 && wq == 0) MLA_TRACE_EV(3, g);
+        // P buffer grp was last read by the V-CTA's PV of tile g-2 (or its epilogue)
+        if (g >= 2 && !wait_bar_warp(&bars->p_free[grp], ((g >> 1) - 1) & 1, abort, true)) {
           failed = true;
           break;
         }
-        const uint32_t rbar = pb ? rPFull1 : rPFull0;
-        const uint32_t prow = rP + pb * kPBytes + row * 128;
+        if (lane == 0 && wq == 0) MLA_TRACE_EV(5, g);
+        const uint32_t prow = rP + row * 128;
 #pragma unroll
         for (int cc = 0; cc < 8; ++cc)
-          ptx::st_async_v4(prow + ((cc ^ (row & 7)) << 4), pk[4 * cc], pk[4 * cc + 1],
-                           pk[4 * cc + 2], pk[4 * cc + 3], rbar);
-        ptx::st_async_b32(rAlpha + (pb * 128 + row) * 4, __float_as_uint(alpha), rbar);
+          ptx::st_async_v4(prow + ((cc ^ (lane & 7)) << 4), pk[4 * cc], pk[4 * cc + 1],
+                           pk[4 * cc + 2], pk[4 * cc + 3], rPFull);
+        ptx::st_async_b32(rAux + row * 4, __float_as_uint(alpha), rPFull);
         const uint32_t wflag = __ballot_sync(0xffffffffu, resc);
-        if (lane == 0) ptx::st_async_b32(rFlags + (pb * 4 + (warp & 3)) * 4, wflag, rbar);
+        if (lane == 0) ptx::st_async_b32(rAux + 512 + wq * 4, wflag, rPFull);
+        if (lane == 0 && wq == 0) MLA_TRACE_EV(6, g);
       }
       if (failed) break;
-      // -- row statistics of the segment -> V-CTA epilogue --
+      // -- segment end: merge the two groups' row sums, statistics -> V-CTA --
       if (seg > 0 && !wait_bar_warp(&bars->stats_free, (seg - 1) & 1, abort, true)) { failed = true; break; }
-      ptx::st_async_b32(rStats + row * 4, __float_as_uint(m_run), rStatsFull);
-      ptx::st_async_b32(rStats + (128 + row) * 4, __float_as_uint(seg_bad ? -1.f : l_run),
-                        rStatsFull);
+      const bool owner = (g_last & 1) == grp;
+      if (!owner) {
+        lm[row] = m_mine;
+        lm[128 + row] = l_mine;
+      }
+      if (!group_bar(0)) { failed = true; break; }
+      if (owner) {
+        const float mo = lm[row], lo = lm[128 + row];
+        const float l = l_mine + ((lo > 0.f) ? lo * ptx::ex2(mo - m_mine) : 0.f);
+        ptx::st_async_b32(rStats + row * 4, __float_as_uint(m_mine), rStatsFull);
+        ptx::st_async_b32(rStats + (128 + row) * 4, __float_as_uint(seg_bad ? -1.f : l),
+                          rStatsFull);
+      }
+      if (!group_bar(1)) { failed = true; break; }
       ++seg;
     }
     if (failed) {
@@ -656,41 +754,42 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     } else {
       // the V-CTA's last remote arrivals land before this CTA may exit
       if (seg > 0) wait_bar_warp(&bars->stats_free, (seg - 1) & 1, abort, true);
-      for (int k = g - 2 < 0 ? 0 : g - 2; k < g; ++k)
-        wait_bar_warp(&bars->p_free[k & 1], (k >> 1) & 1, abort, true);
+      const int gl = g - 1 - ((g - 1 - grp) & 1);  // this group's last tile
+      if (gl >= 0) wait_bar_warp(&bars->p_free[grp], (gl >> 1) & 1, abort, true);
     }
     // items with nothing visible (or an invalid length): o = 0, lse = -inf
-    for (int w = pair; w < W; w += a.npairs) {
-      if (s_prefix[w + 1] != s_prefix[w]) continue;
-      if (row < a.H) {
-        const size_t r = (size_t)w * a.H + row;
-        uint4 *d4 = reinterpret_cast<uint4 *>(a.o_lat + r * kDc);
-        for (int i = 0; i < kDc * 2 / 16; ++i) d4[i] = make_uint4(0, 0, 0, 0);
-        a.lse[r] = -INFINITY;
+    if (grp == 0) {
+      for (int w = pair; w < W; w += a.npairs) {
+        if (item_tiles(a, w) != 0) continue;
+        if (row < a.H) {
+          const size_t r = (size_t)w * a.H + row;
+          uint4 *d4 = reinterpret_cast<uint4 *>(a.o_lat + r * kDc);
+          for (int i = 0; i < kDc * 2 / 16; ++i) d4[i] = make_uint4(0, 0, 0, 0);
+          a.lse[r] = -INFINITY;
+        }
       }
     }
-  } else {
+  } else if (!isS && warp >= 2 && warp <= 5) {
     // ============ V-CTA: rescale and epilogue (warps 2-5) ============
-    const int row = 32 * (warp & 3) + lane;
-    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-    const float *alpha_buf = reinterpret_cast<const float *>(smem + kOffAlpha);
+    const int wq = warp & 3;
+    const int row = 32 * wq + lane;
+    const uint32_t lane_base = (uint32_t)(32 * wq) << 16;
+    const uint8_t *aux = smem + kOffAux;
     const float *stats = reinterpret_cast<const float *>(smem + kOffStats);
-    const uint32_t rStatsFree = ptx::map_to_rank(&bars->stats_free, kRankS);
     SegIter it;
-    it.init(pre, W, t_begin, t_end, w0);
-    int item, lt0, lt1, seg = 0, nev = 0;
+    it.init(&a, W, t_begin, t_end, w0, s0);
+    int item, lt0, lt1, n_vis, seg = 0, nev = 0;
     bool whole, failed = false;
     for (;;) {
       if (!wait_bar_warp(&bars->ev_full, nev & 1, abort)) { failed = true; break; }
       ++nev;
       const int ev = *reinterpret_cast<volatile int *>(&misc->ev_type);
       if ((ev & 15) == kEvDone) break;
+      const int pb = ev >> 4;
       if ((ev & 15) == kEvRescale) {
-        const int pb = ev >> 4;
-        // the factors arrived by st.async from the peer (seen through the
-        // MMA warp's cluster-scope wait)
+        // the factors arrived by st.async (seen through the MMA warp's wait)
         asm volatile("fence.acq_rel.cluster;" ::: "memory");
-        const float al = alpha_buf[pb * 128 + row];
+        const float al = *reinterpret_cast<const volatile float *>(aux + pb * kAuxBytes + row * 4);
         ptx::tc_fence_after();
         if (al != 1.f) {
 #pragma unroll 1
@@ -708,8 +807,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         ptx::mbar_arrive(&bars->ev_done);
         continue;
       }
-      // epilogue of the next segment
-      if (!it.next(&item, &lt0, &lt1, &whole)) { failed = true; break; }
+      // epilogue of the next segment; P buffer pb is free staging
+      if (!it.next(&item, &lt0, &lt1, &whole, &n_vis)) { failed = true; break; }
       if (!wait_bar_warp(&bars->o_full, seg & 1, abort) ||
           !wait_bar_warp(&bars->stats_full, seg & 1, abort, true)) {
         failed = true;
@@ -718,67 +817,86 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
       ptx::tc_fence_after();
       const float m = stats[row], l = stats[128 + row];
       __syncwarp();
-      if (warp == 2 && lane == 0)  // next segment's statistics phase
+      if (wq == 0 && lane == 0)  // next segment's statistics phase
         ptx::mbar_arrive_expect_tx(&bars->stats_full, kStatsBytes);
       if (lane == 0) ptx::mbar_arrive_remote(&bars->stats_free, kRankS);
-      (void)rStatsFree;
       const bool seg_bad = l < 0.f;
-      const bool write_row = row < a.H;
-      const float inv_l = l > 0.f ? 1.f / l : 0.f;
+      const float inv_l = (l > 0.f && !seg_bad) ? 1.f / l : 0.f;
       const float lse_val = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
       const size_t grow = (size_t)item * a.H + row;
+      uint8_t *stg = smem + kOffP + pb * kPBytes + wq * 4096;  // 32 rows x 128 B
+      const int slot_idx = 2 * pair + ((lt0 == 0) ? 1 : 0);    // partial slot
+      // whole items: bf16 rows of o_lat (64 columns = 128 B per chunk);
+      // partial items: fp32 rows of o_part (32 columns = 128 B per chunk)
+      const bool use_tma = !whole || (a.tma_olat && 32 * wq < a.H);
+      const int ncols = whole ? 64 : 32;
+#pragma unroll 1
+      for (int q = 0; q < kDc / ncols; ++q) {
+        uint32_t pk[32];
+        if (whole) {
+          float v[64];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            float t16[16];
+            ptx::tmem_ld16(tmem + lane_base + kTmemO + q * 64 + u * 16, t16);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[u * 16 + i] = t16[i];
+          }
+          ptx::tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) pk[i] = ptx::pack_bf16x2(v[2 * i] * inv_l, v[2 * i + 1] * inv_l);
+        } else {
+          float v[32];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            float t16[16];
+            ptx::tmem_ld16(tmem + lane_base + kTmemO + q * 32 + u * 16, t16);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[u * 16 + i] = t16[i];
+          }
+          ptx::tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) pk[i] = __float_as_uint(v[i] * inv_l);
+        }
+        if (use_tma) {
+          if (lane == 0) ptx::bulk_wait_read_all();  // staging read by the previous store
+          __syncwarp();
+#pragma unroll
+          for (int cc = 0; cc < 8; ++cc)
+            *reinterpret_cast<uint4 *>(stg + lane * 128 + ((cc ^ (lane & 7)) << 4)) =
+                make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            if (whole)
+              ptx::tma_store_2d(&tm_olat, stg, q * 64, (int)((size_t)item * a.H + 32 * wq));
+            else
+              ptx::tma_store_2d(&tm_opart, stg, q * 32, slot_idx * 128 + 32 * wq);
+            ptx::bulk_commit_group();
+          }
+        } else if (row < a.H) {  // rows of an item narrower than 32-row boxes
+          uint4 *d4 = reinterpret_cast<uint4 *>(a.o_lat + grow * kDc + q * 64);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        }
+      }
       if (whole) {
-        __nv_bfloat16 *dst = a.o_lat + grow * kDc;
-#pragma unroll 1
-        for (int q = 0; q < kDc / 32; ++q) {
-          float v0[16], v1[16];
-          ptx::tmem_ld16(tmem + lane_base + kTmemO + q * 32, v0);
-          ptx::tmem_ld16(tmem + lane_base + kTmemO + q * 32 + 16, v1);
-          ptx::tmem_ld_wait();
-          if (write_row) {
-            uint32_t pk[16];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              pk[i] = seg_bad ? 0u : ptx::pack_bf16x2(v0[2 * i] * inv_l, v0[2 * i + 1] * inv_l);
-              pk[8 + i] = seg_bad ? 0u : ptx::pack_bf16x2(v1[2 * i] * inv_l, v1[2 * i + 1] * inv_l);
-            }
-            uint4 *d4 = reinterpret_cast<uint4 *>(dst + q * 32);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-          }
-        }
-        if (write_row) a.lse[grow] = seg_bad ? -INFINITY : lse_val;
+        if (row < a.H) a.lse[grow] = seg_bad ? -INFINITY : lse_val;
       } else {
-        // partial slot: 2*pair for the range's first segment, 2*pair+1 for its last
-        const int slot_idx = 2 * pair + ((lt0 == 0) ? 1 : 0);
-        float *dst = a.o_part + ((size_t)slot_idx * 128 + row) * kDc;
-#pragma unroll 1
-        for (int q = 0; q < kDc / 32; ++q) {
-          float v0[16], v1[16];
-          ptx::tmem_ld16(tmem + lane_base + kTmemO + q * 32, v0);
-          ptx::tmem_ld16(tmem + lane_base + kTmemO + q * 32 + 16, v1);
-          ptx::tmem_ld_wait();
-          if (write_row) {
-            float4 *d4 = reinterpret_cast<float4 *>(dst + q * 32);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              d4[i] = make_float4(v0[4 * i] * inv_l, v0[4 * i + 1] * inv_l, v0[4 * i + 2] * inv_l,
-                                  v0[4 * i + 3] * inv_l);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              d4[4 + i] = make_float4(v1[4 * i] * inv_l, v1[4 * i + 1] * inv_l,
-                                      v1[4 * i + 2] * inv_l, v1[4 * i + 3] * inv_l);
-          }
-        }
-        if (write_row)
+        if (row < a.H)
           a.lse_part[(size_t)slot_idx * 128 + row] =
               seg_bad ? __int_as_float(0x7fc00000) : lse_val;  // NaN poisons the item
       }
       if (seg_bad && row == 0) set_device_error(a.err, kDevBounds);
+      // the staging (a P buffer) is handed back only after the stores read it
+      if (lane == 0) ptx::bulk_wait_read_all();
+      __syncwarp();
       ptx::tc_fence_before();
       ptx::mbar_arrive(&bars->ev_done);
+      if (lane == 0 && wq == 0) MLA_TRACE_EV(7, seg);
       ++seg;
     }
+    if (lane == 0) ptx::bulk_wait_all();
     if (failed) signal_abort(misc, peer);
   }
 
@@ -854,6 +972,7 @@ __global__ void __launch_bounds__(128) combine_tc_kernel(DecodeArgs a) {
 
 size_t part_bytes() { return align_up((size_t)2 * kMaxPairs * 128 * kDc * sizeof(float), 256); }
 size_t lse_part_bytes() { return align_up((size_t)2 * kMaxPairs * 128 * sizeof(float), 256); }
+size_t plan_bytes(int B, int Hq) { return align_up(((size_t)B * Hq + 2) * sizeof(int), 256); }
 
 // Co-resident clusters of two CTAs for this kernel (some GPCs may not fit a
 // whole number of pairs), capped at 74; looked up once per device.
@@ -864,7 +983,7 @@ int pairs_for_device() {
   if (cached[dev] > 0) return cached[dev];
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * kMaxPairs, 1, 1);
-  cfg.blockDim = dim3(192, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = kSmemBytes;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -885,14 +1004,21 @@ int pairs_for_device() {
 
 }  // namespace
 
+#ifdef MLA_TRACE
+extern "C" __attribute__((visibility("default"))) int mla_debug_read_trace(void *host,
+                                                                          size_t bytes) {
+  if (bytes < sizeof(g_trace)) return -1;
+  return cudaMemcpyFromSymbol(host, g_trace, sizeof(g_trace)) == cudaSuccess ? 0 : -1;
+}
+#endif
+
 bool tc_decode_supported(const mla_dims &d) {
   return d.dtype == MLA_BF16 && d.d_c == kDc && d.d_r == kDr && d.block_size == kTile &&
          d.H <= 128;
 }
 
 size_t tc_decode_workspace_bytes(int B, int Hq, const mla_dims &) {
-  const size_t W = (size_t)B * Hq;
-  return kWsHeader + part_bytes() + lse_part_bytes() + align_up((W + 2) * sizeof(int), 256);
+  return kWsHeader + part_bytes() + lse_part_bytes() + plan_bytes(B, Hq);
 }
 
 cudaError_t launch_decode_tc(const void *q_lat, const void *q_rope, const void *cache,
@@ -901,9 +1027,16 @@ cudaError_t launch_decode_tc(const void *q_lat, const void *q_rope, const void *
                              const mla_dims &d, float scale, void *o_lat, float *lse,
                              void *workspace, cudaStream_t st) {
   if ((long)B * Hq > kMaxItems) return cudaErrorNotSupported;
-  CUtensorMap tm_cache;
+  char *ws = static_cast<char *>(workspace);
+  float *o_part = reinterpret_cast<float *>(ws + kWsHeader);
+  const uint64_t rows = (uint64_t)B * Hq * d.H;
+  CUtensorMap tm_cache, tm_olat, tm_opart;
   if (!make_tmap_2d_bf16(&tm_cache, cache, kD, (uint64_t)num_blocks * kTile, kD * 2, 64, 64,
-                         CU_TENSOR_MAP_SWIZZLE_128B))
+                         CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap_2d_bf16(&tm_olat, o_lat, kDc, rows, kDc * 2, 64, 32,
+                         CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap_2d(&tm_opart, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, o_part, kDc,
+                    (uint64_t)2 * kMaxPairs * 128, kDc * 4, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -911,7 +1044,6 @@ cudaError_t launch_decode_tc(const void *q_lat, const void *q_rope, const void *
   if (e != cudaSuccess) return e;
   const int npairs = pairs_for_device();
   if (npairs <= 0) return cudaErrorInvalidDevice;
-  char *ws = static_cast<char *>(workspace);
   DecodeArgs a;
   a.q_lat = static_cast<const __nv_bfloat16 *>(q_lat);
   a.q_rope = static_cast<const __nv_bfloat16 *>(q_rope);
@@ -928,10 +1060,11 @@ cudaError_t launch_decode_tc(const void *q_lat, const void *q_rope, const void *
   a.o_lat = static_cast<__nv_bfloat16 *>(o_lat);
   a.lse = lse;
   a.err = reinterpret_cast<int *>(ws);
-  a.o_part = reinterpret_cast<float *>(ws + kWsHeader);
+  a.o_part = o_part;
   a.lse_part = reinterpret_cast<float *>(ws + kWsHeader + part_bytes());
   a.plan = reinterpret_cast<int *>(ws + kWsHeader + part_bytes() + lse_part_bytes());
-  decode_tc_kernel<<<2 * npairs, 192, kSmemBytes, st>>>(tm_cache, a);
+  a.tma_olat = (d.H % 32) == 0;
+  decode_tc_kernel<<<2 * npairs, kThreads, kSmemBytes, st>>>(tm_cache, tm_olat, tm_opart, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   dim3 cgrid(B * Hq, (d.H + 15) / 16);

@@ -298,6 +298,62 @@ __device__ __forceinline__ void st_cluster_s32(uint32_t addr, int v) {
   asm volatile("st.shared::cluster.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
+// Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned)
+// from this CTA's shared memory into another CTA's shared memory; the
+// mbarrier at `remote_bar` (in the destination CTA) receives the bytes.
+// The copy reads its source through the async proxy: generic-proxy writes of
+// the source need fence_proxy_async_smem() first.
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t remote_dst, const void *local_src,
+                                                  uint32_t bytes, uint32_t remote_bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+      "[%3];" ::"r"(remote_dst),
+      "r"(smem_u32(local_src)), "r"(bytes), "r"(remote_bar)
+      : "memory");
+}
+
+// Bulk copy of `bytes` (multiple of 16, 16-byte aligned) from global memory
+// into this CTA's shared memory, counted on `bar`.
+__device__ __forceinline__ void bulk_load_global(void *dst, const void *src, uint32_t bytes,
+                                                 uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// TMA store of one tensor-map box from this CTA's shared memory (bulk group).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void *src, int x,
+                                             int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(smem_u32(src)), "r"(x), "r"(y)
+      : "memory");
+}
+
+// Make generic-proxy global writes visible to the async proxy (a later bulk
+// copy or TMA that reads them).
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+__device__ __forceinline__ void bulk_commit_group() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Wait until every bulk copy this thread committed has finished reading its
+// source (the copies themselves may still be in flight).
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Wait until every bulk copy this thread committed has completed.
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 // Arrive (with an expected byte count) on this CTA's mbarrier, no return value.
 __device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
   mbar_arrive_expect_tx(bar, bytes);

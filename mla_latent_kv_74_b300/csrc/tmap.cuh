@@ -25,21 +25,28 @@ inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// A 2-D bf16 tensor [outer][inner] with rows `row_bytes` apart, read in boxes
-// of box_inner x box_outer elements.  Out-of-range elements read as zero.
-inline bool make_tmap_2d_bf16(CUtensorMap *map, const void *base, uint64_t inner, uint64_t outer,
-                              uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
-                              CUtensorMapSwizzle swizzle) {
+// A 2-D tensor [outer][inner] with rows `row_bytes` apart, moved in boxes of
+// box_inner x box_outer elements.  Out-of-range elements read as zero and
+// are not written.
+inline bool make_tmap_2d(CUtensorMap *map, CUtensorMapDataType type, const void *base,
+                         uint64_t inner, uint64_t outer, uint64_t row_bytes, uint32_t box_inner,
+                         uint32_t box_outer, CUtensorMapSwizzle swizzle) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
   cuuint64_t dims[2] = {inner, outer};
   cuuint64_t strides[1] = {row_bytes};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t estr[2] = {1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
-             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
-         CUDA_SUCCESS;
+  return enc(map, type, 2, const_cast<void *>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+inline bool make_tmap_2d_bf16(CUtensorMap *map, const void *base, uint64_t inner, uint64_t outer,
+                              uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+                              CUtensorMapSwizzle swizzle) {
+  return make_tmap_2d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, inner, outer, row_bytes,
+                      box_inner, box_outer, swizzle);
 }
 
 }  // namespace mla
