@@ -171,7 +171,7 @@ def run_ours(args, rank, world, device):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream(device)
 
-    def step(x):
+    def step(x, ev):
         mla.mla_append_cache(cache, inp["num_blocks"], x["block_table"], x["seqlens"],
                              x["c_kv_new"], x["k_r_new"], dims, stream)
         mla.mla_absorb_query(x["q_nope"], dev["W_UK"], q_lat, dims, stream)
@@ -182,10 +182,13 @@ def run_ours(args, rank, world, device):
         mla.mla_out_proj(o_lat, dev["W_UV"], out, dims, stream)
 
     # ---- device-resident timing -------------------------------------------
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    # All timed steps are enqueued before one synchronisation, so the GPU
+    # never idles between a step's kernels waiting for the host to prepare
+    # the next call (that gap would land inside the measured intervals).
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     for _ in range(args.warmup):
         flush.zero_()
-        step(dev)
+        step(dev, evs[0])
     torch.cuda.synchronize()
     status = mla.mla_get_error(ws)
     if status != 0:
@@ -197,15 +200,16 @@ def run_ours(args, rank, world, device):
     torch.cuda.synchronize()
     with ClockSampler(smi_index(device.index)) as clocks:
         t_wall = time.perf_counter()
-        for _ in range(args.steps):
+        for it in range(args.steps):
+            ev = evs[it]
             flush.zero_()
             ev[0].record(stream)
-            step(dev)
+            step(dev, ev)
             ev[3].record(stream)
-            ev[3].synchronize()
+        torch.cuda.synchronize()
+        for ev in evs:
             step_ms.append(ev[0].elapsed_time(ev[3]))
             dec_ms.append(ev[1].elapsed_time(ev[2]))
-        torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall
     if world > 1:
         torch.distributed.barrier()
@@ -227,7 +231,7 @@ def run_ours(args, rank, world, device):
         e0.record(stream)
         for k in host_keys:
             staged[k].copy_(pinned[k], non_blocking=True)
-        step(staged)
+        step(staged, evs[0])
         out_host.copy_(out, non_blocking=True)
         e1.record(stream)
         e1.synchronize()

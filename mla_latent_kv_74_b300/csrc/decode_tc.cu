@@ -99,7 +99,11 @@ constexpr uint32_t kOffAux = kOffP + 2 * kPBytes;
 constexpr uint32_t kOffStats = kOffAux + 2 * kAuxBytes;  // m[128], l[128]
 constexpr uint32_t kStatsBytes = 2 * 128 * 4;
 constexpr uint32_t kVEnd = kOffStats + kStatsBytes;
-constexpr uint32_t kMsgBytes = kPBytes + kAuxBytes;  // one P message
+// A P tile travels as two messages, tokens 0-31 (with the rescale factors
+// and flags) and tokens 32-63, so the PV can start on the first half while
+// the second is in flight and each half-buffer is freed after its k-steps.
+constexpr uint32_t kMsgBytesA = kPBytes / 2 + kAuxBytes;
+constexpr uint32_t kMsgBytesB = kPBytes / 2;
 // both
 constexpr uint32_t kOffBars = kSEnd > kVEnd ? kSEnd : kVEnd;
 static_assert(kOffP % 1024 == 0, "P buffers must be 1024-byte aligned");
@@ -113,9 +117,9 @@ struct Bars {
   uint64_t q_full, q_free;                 // S: query in TMEM / QK^T of a segment done
   uint64_t m_ready[2];                     // S: group i published its tile's maximum
   uint64_t seg_sync[2];                    // S: both softmax groups at a segment end
-  uint64_t p_free[2];                      // S: V-CTA done with P buffer i
+  uint64_t p_free[4];                      // S: V-CTA done with half h of P buffer i (2i+h)
   uint64_t stats_free;                     // S: V-CTA read the statistics
-  uint64_t p_full[2];                      // V: P message i arrived
+  uint64_t p_full[4];                      // V: half h of P message i arrived (2i+h)
   uint64_t stats_full;                     // V: row statistics arrived
   uint64_t o_full, pv_done;                // V: accumulator complete
   uint64_t ev_full, ev_done;               // V: MMA warp <-> correction warps
@@ -153,7 +157,6 @@ struct DecodeArgs {
   float *lse_part;  // [2 * kMaxPairs][128]
   int *plan;        // [0] = tiles per pair, [1..W+1] = prefix of tiles per item
   int *err;
-  int tma_olat;     // o_lat rows can be written with 32-row TMA boxes (H % 32 == 0)
 };
 
 #ifdef MLA_TRACE
@@ -165,6 +168,10 @@ struct DecodeArgs {
 // free, 6 S: P sent, 7 per segment: S query loaded / V epilogue done.
 constexpr int kTraceTiles = 512, kTraceEvents = 8, kTracePairs = 2;
 __device__ unsigned long long g_trace[kTracePairs][2][kTraceEvents][kTraceTiles];
+// per CTA: kernel entry, range start (after setup), end of work
+__device__ unsigned long long g_trace_cta[2 * kMaxPairs][3];
+#define MLA_TRACE_CTA(k) \
+  do { if (threadIdx.x == 0) g_trace_cta[blockIdx.x][k] = ptx::globaltimer_ns(); } while (0)
 __device__ __forceinline__ void trace_ev(int pair, int npairs, uint32_t rank, int ev, int g) {
   const int slot = pair == 0 ? 0 : (pair == npairs / 2 ? 1 : -1);
   if (slot >= 0 && g >= 0 && g < kTraceTiles) g_trace[slot][rank][ev][g] = ptx::globaltimer_ns();
@@ -172,6 +179,7 @@ __device__ __forceinline__ void trace_ev(int pair, int npairs, uint32_t rank, in
 #define MLA_TRACE_EV(ev, g) trace_ev(pair, a.npairs, rank, (ev), (g))
 #else
 #define MLA_TRACE_EV(ev, g) ((void)0)
+#define MLA_TRACE_CTA(k) ((void)0)
 #endif
 
 __device__ __forceinline__ int visible_len(const DecodeArgs &a, int w, bool *bad) {
@@ -267,9 +275,7 @@ __device__ __forceinline__ void signal_abort(Misc *misc, uint32_t peer) {
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    decode_tc_kernel(const __grid_constant__ CUtensorMap tm_cache,
-                     const __grid_constant__ CUtensorMap tm_olat,
-                     const __grid_constant__ CUtensorMap tm_opart, DecodeArgs a) {
+    decode_tc_kernel(const __grid_constant__ CUtensorMap tm_cache, DecodeArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
   Bars *bars = reinterpret_cast<Bars *>(smem + kOffBars);
   Misc *misc = reinterpret_cast<Misc *>(smem + kOffMisc);
@@ -281,6 +287,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int pair = blockIdx.x >> 1;
   const int W = a.B * a.Hq;
   volatile int *abort = &misc->abort;
+  MLA_TRACE_CTA(0);
 
   // ---- setup: barriers, TMEM, this pair's tile range ----
   if (threadIdx.x == 0) {
@@ -302,8 +309,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(&bars->m_ready[s], 128);
       ptx::mbar_init(&bars->seg_sync[s], 256);
-      ptx::mbar_init(&bars->p_free[s], 1);
-      ptx::mbar_init(&bars->p_full[s], 1);
+      ptx::mbar_init(&bars->p_free[2 * s], 1);
+      ptx::mbar_init(&bars->p_free[2 * s + 1], 1);
+      ptx::mbar_init(&bars->p_full[2 * s], 1);
+      ptx::mbar_init(&bars->p_full[2 * s + 1], 1);
       ptx::mbar_init(&bars->drain[s], 1);
     }
     ptx::mbar_init(&bars->stats_free, 4);
@@ -314,18 +323,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     ptx::mbar_init(&bars->ev_done, 128);
     ptx::fence_mbar_init();
     if (!isS) {  // the first message phases the S-CTA fills
-      ptx::mbar_arrive_expect_tx(&bars->p_full[0], kMsgBytes);
-      ptx::mbar_arrive_expect_tx(&bars->p_full[1], kMsgBytes);
+      for (int i = 0; i < 2; ++i) {
+        ptx::mbar_arrive_expect_tx(&bars->p_full[2 * i], kMsgBytesA);
+        ptx::mbar_arrive_expect_tx(&bars->p_full[2 * i + 1], kMsgBytesB);
+      }
       ptx::mbar_arrive_expect_tx(&bars->stats_full, kStatsBytes);
     }
   }
-  if (warp == 0 && lane == 0) {
-    ptx::tma_prefetch_desc(&tm_cache);
-    if (!isS) {
-      ptx::tma_prefetch_desc(&tm_olat);
-      ptx::tma_prefetch_desc(&tm_opart);
-    }
-  }
+  if (warp == 0 && lane == 0) ptx::tma_prefetch_desc(&tm_cache);
   if (warp == 1) ptx::tmem_alloc(&misc->tmem, 512);
   if (isS) {
     // tiles per item -> scan (scratch in the ring) -> this pair's range
@@ -384,6 +389,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   const uint32_t tmem = misc->tmem;
   const bool bad_smem = misc->bad_smem != 0;
+  MLA_TRACE_CTA(1);
   int t_begin, t_end, w0, s0;
   if (isS) {
     t_begin = misc->t_begin;
@@ -505,7 +511,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const int st = g % kStages, pb = g & 1;
           if (!wait_bar(&bars->full[st], (g / kStages) & 1, abort)) { failed = true; break; }
           MLA_TRACE_EV(1, g);
-          if (!wait_bar_cl(&bars->p_full[pb], (g >> 1) & 1, abort)) { failed = true; break; }
+          if (!wait_bar_cl(&bars->p_full[2 * pb], (g >> 1) & 1, abort)) { failed = true; break; }
           MLA_TRACE_EV(2, g);
           const volatile uint32_t *fl =
               reinterpret_cast<const volatile uint32_t *>(aux + pb * kAuxBytes + 512);
@@ -517,31 +523,44 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             ++npv;
             if (!post(kEvRescale | (pb << 4))) { failed = true; break; }
           }
-          // the next message into this buffer comes after the PV below
-          ptx::mbar_arrive_expect_tx(&bars->p_full[pb], kMsgBytes);
-          ptx::fence_proxy_async_smem();  // P arrived by st.async (generic proxy)
-          ptx::tc_fence_after();
           const uint64_t ad0 = p_desc + (uint64_t)((pb * kPBytes) >> 4);
           const uint64_t bd0 = ring_desc + (uint64_t)((st * kVStage) >> 4);
 #pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk) {
+          for (int half = 0; half < 2; ++half) {
+            if (half == 1 &&
+                !wait_bar_cl(&bars->p_full[2 * pb + 1], (g >> 1) & 1, abort)) {
+              failed = true;
+              break;
+            }
+            // the next message into this half-buffer comes after the MMAs below
+            ptx::mbar_arrive_expect_tx(&bars->p_full[2 * pb + half],
+                                       half ? kMsgBytesB : kMsgBytesA);
+            ptx::fence_proxy_async_smem();  // P arrived by st.async (generic proxy)
+            ptx::tc_fence_after();
 #pragma unroll
-            for (int h = 0; h < 2; ++h)
-              ptx::mma_bf16(tmem + kTmemO + h * 256, ad0 + (uint64_t)((kk * 32) >> 4),
-                            bd0 + (uint64_t)((h * 4 * kBox + kk * 2048) >> 4), idesc,
-                            (lt == lt0 && kk == 0) ? 0u : 1u);
+            for (int k2 = 0; k2 < 2; ++k2) {
+              const int kk = 2 * half + k2;
+#pragma unroll
+              for (int h = 0; h < 2; ++h)
+                ptx::mma_bf16(tmem + kTmemO + h * 256, ad0 + (uint64_t)((kk * 32) >> 4),
+                              bd0 + (uint64_t)((h * 4 * kBox + kk * 2048) >> 4), idesc,
+                              (lt == lt0 && kk == 0) ? 0u : 1u);
+            }
+            // the last tile's P buffer becomes the epilogue's staging
+            if (lt != lt1 - 1) ptx::mma_commit_mc(&bars->p_free[2 * pb + half], kMaskS);
           }
+          if (failed) break;
           ptx::mma_commit(&bars->empty[st]);
-          // the last tile's P buffer becomes the epilogue's staging
-          if (lt != lt1 - 1) ptx::mma_commit_mc(&bars->p_free[pb], kMaskS);
           MLA_TRACE_EV(3, g);
         }
         if (failed) break;
         ptx::mma_commit(&bars->o_full);
         if (!wait_bar(&bars->o_full, seg & 1, abort)) { failed = true; break; }
         const int last_pb = (g - 1) & 1;
+        MLA_TRACE_EV(7, 256 + seg);
         if (!post(kEvEpilogue | (last_pb << 4))) { failed = true; break; }
-        ptx::mbar_arrive_remote(&bars->p_free[last_pb], kRankS);  // staging handed back
+        ptx::mbar_arrive_remote(&bars->p_free[2 * last_pb], kRankS);  // staging handed back
+        ptx::mbar_arrive_remote(&bars->p_free[2 * last_pb + 1], kRankS);
         ++seg;
       }
       misc->ev_type = kEvDone;
@@ -562,7 +581,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     float *lm = reinterpret_cast<float *>(smem + kOffLM);
     const uint32_t rP = ptx::map_to_rank(smem + kOffP + grp * kPBytes, kRankV);
     const uint32_t rAux = ptx::map_to_rank(smem + kOffAux + grp * kAuxBytes, kRankV);
-    const uint32_t rPFull = ptx::map_to_rank(&bars->p_full[grp], kRankV);
+    const uint32_t rPFullA = ptx::map_to_rank(&bars->p_full[2 * grp], kRankV);
+    const uint32_t rPFullB = ptx::map_to_rank(&bars->p_full[2 * grp + 1], kRankV);
     const uint32_t rStats = ptx::map_to_rank(smem + kOffStats, kRankV);
     const uint32_t rStatsFull = ptx::map_to_rank(&bars->stats_full, kRankV);
     const float c = a.scale_log2;
@@ -613,17 +633,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
           }
         };
-        uint4 cur[3][4], nxt[3][4];
+        // three rounds of 6 chunks, all of a round's loads in flight at once
 #pragma unroll
-        for (int j = 0; j < 3; ++j) load_chunk(j, cur[j]);
+        for (int rd = 0; rd < 3; ++rd) {
+          uint4 cur[6][4];
 #pragma unroll
-        for (int gp = 0; gp < 6; ++gp) {
-          if (gp < 5) {
+          for (int j = 0; j < 6; ++j) load_chunk(6 * rd + j, cur[j]);
 #pragma unroll
-            for (int j = 0; j < 3; ++j) load_chunk(3 * (gp + 1) + j, nxt[j]);
-          }
-#pragma unroll
-          for (int j = 0; j < 3; ++j) {
+          for (int j = 0; j < 6; ++j) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               const int r = 8 * i + (lane >> 2), part = lane & 3;
@@ -639,14 +656,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               v[4 * k + 2] = x.z;
               v[4 * k + 3] = x.w;
             }
-            ptx::tmem_st16_nc(tmem + lane_base + kTmemQ + (3 * gp + j) * 16, v);
+            ptx::tmem_st16_nc(tmem + lane_base + kTmemQ + (6 * rd + j) * 16, v);
             __syncwarp();
-          }
-          if (gp < 5) {
-#pragma unroll
-            for (int j = 0; j < 3; ++j)
-#pragma unroll
-              for (int i = 0; i < 4; ++i) cur[j][i] = nxt[j][i];
           }
         }
         ptx::tmem_st_wait();
@@ -657,6 +668,46 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
       // this group's row sum over its tiles of the segment, relative to m_mine
       float m_mine = -INFINITY, l_mine = 0.f;
+      // Software pipeline: a tile's maximum is published as soon as its
+      // scores are read, before this group ships the P of its previous tile
+      // (held in registers), so the other group never waits on a transfer.
+      uint32_t pk_prev[32];
+      float alpha_prev = 1.f;
+      bool resc_prev = false;
+      int g_prev = -1;
+      auto send_prev = [&]() -> bool {
+        if (g_prev < 0) return true;
+        const uint32_t prow = rP + row * 128;
+        const int ph = ((g_prev >> 1) - 1) & 1;
+        // half 0 (tokens 0-31) with the rescale factors and flags; each half
+        // of buffer grp was last read by the V-CTA's PV of tile g_prev-2
+        if (g_prev >= 2 && !wait_bar_warp(&bars->p_free[2 * grp], ph, abort, true)) return false;
+        if (lane == 0 && wq == 0) MLA_TRACE_EV(5, g_prev);
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc)
+          ptx::st_async_v4(prow + ((cc ^ (lane & 7)) << 4), pk_prev[4 * cc], pk_prev[4 * cc + 1],
+                           pk_prev[4 * cc + 2], pk_prev[4 * cc + 3], rPFullA);
+        {  // the warp's 32 factors as 8 vector stores (lanes 0-7)
+          float a4[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) a4[j] = __shfl_sync(0xffffffffu, alpha_prev, (4 * lane + j) & 31);
+          if (lane < 8)
+            ptx::st_async_v4(rAux + (32 * wq + 4 * lane) * 4, __float_as_uint(a4[0]),
+                             __float_as_uint(a4[1]), __float_as_uint(a4[2]), __float_as_uint(a4[3]),
+                             rPFullA);
+        }
+        const uint32_t wflag = __ballot_sync(0xffffffffu, resc_prev);
+        if (lane == 0) ptx::st_async_b32(rAux + 512 + wq * 4, wflag, rPFullA);
+        // half 1 (tokens 32-63)
+        if (g_prev >= 2 && !wait_bar_warp(&bars->p_free[2 * grp + 1], ph, abort, true)) return false;
+#pragma unroll
+        for (int cc = 4; cc < 8; ++cc)
+          ptx::st_async_v4(prow + ((cc ^ (lane & 7)) << 4), pk_prev[4 * cc], pk_prev[4 * cc + 1],
+                           pk_prev[4 * cc + 2], pk_prev[4 * cc + 3], rPFullB);
+        if (lane == 0 && wq == 0) MLA_TRACE_EV(6, g_prev);
+        g_prev = -1;
+        return true;
+      };
       for (int lt = lt0; lt < lt1; ++lt, ++g) {
         if ((g & 1) != grp) continue;
         const int sb = g % 3;
@@ -699,37 +750,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         m_dec[row] = m_use;
         ptx::mbar_arrive(&bars->m_ready[grp]);
-        uint32_t pk[32];
+        if (!send_prev()) { failed = true; break; }
         float lsum = 0.f;
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           const float p0 = ptx::ex2(fmaf(s[2 * i], c, -m_use));
           const float p1 = ptx::ex2(fmaf(s[2 * i + 1], c, -m_use));
           lsum += p0 + p1;
-          pk[i] = ptx::pack_bf16x2(p0, p1);
+          pk_prev[i] = ptx::pack_bf16x2(p0, p1);
         }
+        alpha_prev = alpha;
+        resc_prev = resc;
+        g_prev = g;
         if (m_use != m_mine) {  // the maximum moved since this group's last tile
           l_mine = (m_mine == -INFINITY) ? 0.f : l_mine * ptx::ex2(m_mine - m_use);
           m_mine = m_use;
         }
         l_mine += lsum;
         if (lane == 0 && wq == 0) MLA_TRACE_EV(3, g);
-        // P buffer grp was last read by the V-CTA's PV of tile g-2 (or its epilogue)
-        if (g >= 2 && !wait_bar_warp(&bars->p_free[grp], ((g >> 1) - 1) & 1, abort, true)) {
-          failed = true;
-          break;
-        }
-        if (lane == 0 && wq == 0) MLA_TRACE_EV(5, g);
-        const uint32_t prow = rP + row * 128;
-#pragma unroll
-        for (int cc = 0; cc < 8; ++cc)
-          ptx::st_async_v4(prow + ((cc ^ (lane & 7)) << 4), pk[4 * cc], pk[4 * cc + 1],
-                           pk[4 * cc + 2], pk[4 * cc + 3], rPFull);
-        ptx::st_async_b32(rAux + row * 4, __float_as_uint(alpha), rPFull);
-        const uint32_t wflag = __ballot_sync(0xffffffffu, resc);
-        if (lane == 0) ptx::st_async_b32(rAux + 512 + wq * 4, wflag, rPFull);
-        if (lane == 0 && wq == 0) MLA_TRACE_EV(6, g);
       }
+      if (!failed && !send_prev()) failed = true;
       if (failed) break;
       // -- segment end: merge the two groups' row sums, statistics -> V-CTA --
       if (seg > 0 && !wait_bar_warp(&bars->stats_free, (seg - 1) & 1, abort, true)) { failed = true; break; }
@@ -745,6 +785,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         ptx::st_async_b32(rStats + row * 4, __float_as_uint(m_mine), rStatsFull);
         ptx::st_async_b32(rStats + (128 + row) * 4, __float_as_uint(seg_bad ? -1.f : l),
                           rStatsFull);
+        if (lane == 0 && wq == 0) MLA_TRACE_EV(7, 128 + seg);
       }
       if (!group_bar(1)) { failed = true; break; }
       ++seg;
@@ -755,7 +796,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // the V-CTA's last remote arrivals land before this CTA may exit
       if (seg > 0) wait_bar_warp(&bars->stats_free, (seg - 1) & 1, abort, true);
       const int gl = g - 1 - ((g - 1 - grp) & 1);  // this group's last tile
-      if (gl >= 0) wait_bar_warp(&bars->p_free[grp], (gl >> 1) & 1, abort, true);
+      if (gl >= 0) {
+        wait_bar_warp(&bars->p_free[2 * grp], (gl >> 1) & 1, abort, true);
+        wait_bar_warp(&bars->p_free[2 * grp + 1], (gl >> 1) & 1, abort, true);
+      }
     }
     // items with nothing visible (or an invalid length): o = 0, lse = -inf
     if (grp == 0) {
@@ -815,6 +859,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         break;
       }
       ptx::tc_fence_after();
+      if (lane == 0 && wq == 0) MLA_TRACE_EV(7, 128 + seg);
       const float m = stats[row], l = stats[128 + row];
       __syncwarp();
       if (wq == 0 && lane == 0)  // next segment's statistics phase
@@ -824,60 +869,58 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const float inv_l = (l > 0.f && !seg_bad) ? 1.f / l : 0.f;
       const float lse_val = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
       const size_t grow = (size_t)item * a.H + row;
+      // O rows leave through this warp's 4 KB of the P buffer pb (free staging):
+      // each thread writes its row's 128-byte chunk (128B-swizzled, no bank
+      // conflicts), then each instruction stores four whole 128-byte row
+      // pieces to global memory.
       uint8_t *stg = smem + kOffP + pb * kPBytes + wq * 4096;  // 32 rows x 128 B
       const int slot_idx = 2 * pair + ((lt0 == 0) ? 1 : 0);    // partial slot
-      // whole items: bf16 rows of o_lat (64 columns = 128 B per chunk);
-      // partial items: fp32 rows of o_part (32 columns = 128 B per chunk)
-      const bool use_tma = !whole || (a.tma_olat && 32 * wq < a.H);
-      const int ncols = whole ? 64 : 32;
-#pragma unroll 1
-      for (int q = 0; q < kDc / ncols; ++q) {
-        uint32_t pk[32];
-        if (whole) {
-          float v[64];
+      // whole items: bf16 rows of o_lat; partial items: fp32 rows of o_part
+      uint8_t *dst_base = whole
+          ? reinterpret_cast<uint8_t *>(a.o_lat + ((size_t)item * a.H + 32 * wq) * kDc)
+          : reinterpret_cast<uint8_t *>(a.o_part + ((size_t)slot_idx * 128 + 32 * wq) * kDc);
+      const size_t dst_row_bytes = whole ? kDc * 2 : kDc * 4;
+      const int rows_here = whole ? min(32, a.H - 32 * wq) : 32;  // rows of this item
+      // one staged 128-byte piece per row: thread = row in, lane = 16 B out
+      auto flush_piece = [&](const uint32_t (&pk)[32], size_t byte_off) {
+        __syncwarp();  // the previous piece's reads of the staging are done
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            float t16[16];
-            ptx::tmem_ld16(tmem + lane_base + kTmemO + q * 64 + u * 16, t16);
+        for (int cc = 0; cc < 8; ++cc)
+          *reinterpret_cast<uint4 *>(stg + lane * 128 + ((cc ^ (lane & 7)) << 4)) =
+              make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+        __syncwarp();
 #pragma unroll
-            for (int i = 0; i < 16; ++i) v[u * 16 + i] = t16[i];
+        for (int i = 0; i < 8; ++i) {
+          const int r = 4 * i + (lane >> 3), k = lane & 7;
+          if (r < rows_here) {
+            const uint4 x = *reinterpret_cast<const uint4 *>(stg + r * 128 + ((k ^ (r & 7)) << 4));
+            *reinterpret_cast<uint4 *>(dst_base + r * dst_row_bytes + byte_off + k * 16) = x;
           }
-          ptx::tmem_ld_wait();
+        }
+      };
+#pragma unroll 1
+      for (int q = 0; q < kDc / 64; ++q) {  // 64 TMEM columns per wait
+        float v[64];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          float t16[16];
+          ptx::tmem_ld16(tmem + lane_base + kTmemO + q * 64 + u * 16, t16);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v[u * 16 + i] = t16[i];
+        }
+        ptx::tmem_ld_wait();
+        uint32_t pk[32];
+        if (whole) {  // 64 bf16 = one 128-byte piece
 #pragma unroll
           for (int i = 0; i < 32; ++i) pk[i] = ptx::pack_bf16x2(v[2 * i] * inv_l, v[2 * i + 1] * inv_l);
-        } else {
-          float v[32];
+          flush_piece(pk, (size_t)q * 128);
+        } else {  // 64 fp32 = two 128-byte pieces
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            float t16[16];
-            ptx::tmem_ld16(tmem + lane_base + kTmemO + q * 32 + u * 16, t16);
+          for (int hp = 0; hp < 2; ++hp) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) v[u * 16 + i] = t16[i];
+            for (int i = 0; i < 32; ++i) pk[i] = __float_as_uint(v[32 * hp + i] * inv_l);
+            flush_piece(pk, (size_t)q * 256 + hp * 128);
           }
-          ptx::tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) pk[i] = __float_as_uint(v[i] * inv_l);
-        }
-        if (use_tma) {
-          if (lane == 0) ptx::bulk_wait_read_all();  // staging read by the previous store
-          __syncwarp();
-#pragma unroll
-          for (int cc = 0; cc < 8; ++cc)
-            *reinterpret_cast<uint4 *>(stg + lane * 128 + ((cc ^ (lane & 7)) << 4)) =
-                make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
-          ptx::fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            if (whole)
-              ptx::tma_store_2d(&tm_olat, stg, q * 64, (int)((size_t)item * a.H + 32 * wq));
-            else
-              ptx::tma_store_2d(&tm_opart, stg, q * 32, slot_idx * 128 + 32 * wq);
-            ptx::bulk_commit_group();
-          }
-        } else if (row < a.H) {  // rows of an item narrower than 32-row boxes
-          uint4 *d4 = reinterpret_cast<uint4 *>(a.o_lat + grow * kDc + q * 64);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
         }
       }
       if (whole) {
@@ -888,15 +931,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               seg_bad ? __int_as_float(0x7fc00000) : lse_val;  // NaN poisons the item
       }
       if (seg_bad && row == 0) set_device_error(a.err, kDevBounds);
-      // the staging (a P buffer) is handed back only after the stores read it
-      if (lane == 0) ptx::bulk_wait_read_all();
       __syncwarp();
       ptx::tc_fence_before();
       ptx::mbar_arrive(&bars->ev_done);
       if (lane == 0 && wq == 0) MLA_TRACE_EV(7, seg);
       ++seg;
     }
-    if (lane == 0) ptx::bulk_wait_all();
     if (failed) signal_abort(misc, peer);
   }
 
@@ -904,6 +944,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   __syncwarp();
   ptx::tc_fence_before();
   __syncthreads();
+  MLA_TRACE_CTA(2);
   if (misc->abort) {
     if (threadIdx.x == 0) set_device_error(a.err, kDevTimeout);
     __nanosleep(20000);  // copies the peer issued before it stopped have landed
@@ -913,61 +954,78 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (warp == 1) ptx::tmem_dealloc(tmem, 512);
 }
 
-// Merge the partial pieces of every item that was cut between pairs.
-// grid (W items, H / 16 row groups); 128 threads; non-split items exit.
-__global__ void __launch_bounds__(128) combine_tc_kernel(DecodeArgs a) {
-  const int w = blockIdx.x;
+// Merge the partial pieces of every item that was cut between pairs
+// (log-sum-exp weights): one warp per output row (item w, head h), eight rows
+// per block.  Lane i weighs piece p0 + i (pieces of one item <= 32 per round),
+// then each lane accumulates 16 consecutive columns over the pieces, so every
+// piece row is read as 2 KB of coalesced loads.  Rows of items written
+// directly by their pair return at once.
+constexpr int kCombineRows = 8;
+__global__ void __launch_bounds__(32 * kCombineRows) combine_tc_kernel(DecodeArgs a) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long rowg = (long)blockIdx.x * kCombineRows + warp;
+  const int W = a.B * a.Hq;
+  if (rowg >= (long)W * a.H) return;
+  const int w = (int)(rowg / a.H), h = (int)(rowg % a.H);
   const int per = a.plan[0];
   const int s = a.plan[1 + w], e = a.plan[2 + w];
   if (e <= s || per <= 0) return;
   const int p0 = s / per, p1 = (e - 1) / per;
   if (p0 == p1) return;  // written directly by its pair
-  const int h0 = blockIdx.y * 16;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int hh = warp; hh < 16; hh += 4) {
-    const int h = h0 + hh;
-    if (h >= a.H) break;
-    float mx = -INFINITY;
-    bool poison = false;
-    for (int p = p0; p <= p1; ++p) {
-      const int slot = 2 * p + ((s < p * per) ? 0 : 1);
-      const float v = a.lse_part[(size_t)slot * 128 + h];
-      poison |= isnan(v);
-      mx = fmaxf(mx, v);
-    }
-    const int row = w * a.H + h;
-    __nv_bfloat16 *dst = a.o_lat + (size_t)row * kDc;
-    if (poison || mx == -INFINITY) {
-      for (int c = lane; c < kDc; c += 32) dst[c] = __float2bfloat16_rn(0.f);
-      if (lane == 0) a.lse[row] = -INFINITY;
-      continue;
-    }
-    float sum = 0.f;
-    for (int p = p0; p <= p1; ++p) {
-      const int slot = 2 * p + ((s < p * per) ? 0 : 1);
-      sum += expf(a.lse_part[(size_t)slot * 128 + h] - mx);
-    }
-    const float inv = 1.f / sum;
-    for (int c4 = lane; c4 < kDc / 4; c4 += 32) {
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int p = p0; p <= p1; ++p) {
-        const int slot = 2 * p + ((s < p * per) ? 0 : 1);
-        const float wgt = expf(a.lse_part[(size_t)slot * 128 + h] - mx) * inv;
-        const float4 v = reinterpret_cast<const float4 *>(a.o_part + ((size_t)slot * 128 + h) * kDc)[c4];
-        acc.x = fmaf(wgt, v.x, acc.x);
-        acc.y = fmaf(wgt, v.y, acc.y);
-        acc.z = fmaf(wgt, v.z, acc.z);
-        acc.w = fmaf(wgt, v.w, acc.w);
-      }
-      uint2 pk;
-      pk.x = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(acc.x)) |
-             ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(acc.y)) << 16);
-      pk.y = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(acc.z)) |
-             ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(acc.w)) << 16);
-      reinterpret_cast<uint2 *>(dst)[c4] = pk;
-    }
-    if (lane == 0) a.lse[row] = mx + logf(sum);
+  auto slot_of = [&](int p) { return 2 * p + ((s < p * per) ? 0 : 1); };
+  // maximum and sum of exp(lse) over the pieces
+  float mx = -INFINITY;
+  bool poison = false;
+  for (int p = p0 + lane; p <= p1; p += 32) {
+    const float v = a.lse_part[(size_t)slot_of(p) * 128 + h];
+    poison |= isnan(v);
+    mx = fmaxf(mx, v);
   }
+#pragma unroll
+  for (int off = 16; off; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  poison = __any_sync(0xffffffffu, poison);
+  __nv_bfloat16 *dst = a.o_lat + (size_t)rowg * kDc;
+  if (poison || mx == -INFINITY) {
+    reinterpret_cast<uint4 *>(dst)[lane] = make_uint4(0, 0, 0, 0);
+    reinterpret_cast<uint4 *>(dst)[lane + 32] = make_uint4(0, 0, 0, 0);
+    if (lane == 0) a.lse[rowg] = -INFINITY;
+    return;
+  }
+  float sum = 0.f;
+  for (int p = p0 + lane; p <= p1; p += 32)
+    sum += expf(a.lse_part[(size_t)slot_of(p) * 128 + h] - mx);
+#pragma unroll
+  for (int off = 16; off; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+  const float inv = 1.f / sum;
+  float acc[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+  for (int base = p0; base <= p1; base += 32) {
+    const int p_l = base + lane;
+    const float wl = p_l <= p1 ? expf(a.lse_part[(size_t)slot_of(p_l) * 128 + h] - mx) * inv : 0.f;
+    const int n = min(32, p1 - base + 1);
+    for (int j = 0; j < n; ++j) {
+      const float wgt = __shfl_sync(0xffffffffu, wl, j);
+      const float4 *src =
+          reinterpret_cast<const float4 *>(a.o_part + ((size_t)slot_of(base + j) * 128 + h) * kDc) +
+          lane * 4;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float4 v = src[q];
+        acc[4 * q] = fmaf(wgt, v.x, acc[4 * q]);
+        acc[4 * q + 1] = fmaf(wgt, v.y, acc[4 * q + 1]);
+        acc[4 * q + 2] = fmaf(wgt, v.z, acc[4 * q + 2]);
+        acc[4 * q + 3] = fmaf(wgt, v.w, acc[4 * q + 3]);
+      }
+    }
+  }
+  uint32_t pk[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) pk[i] = ptx::pack_bf16x2(acc[2 * i], acc[2 * i + 1]);
+  uint4 *d4 = reinterpret_cast<uint4 *>(dst) + lane * 2;
+  d4[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+  d4[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+  if (lane == 0) a.lse[rowg] = mx + logf(sum);
 }
 
 size_t part_bytes() { return align_up((size_t)2 * kMaxPairs * 128 * kDc * sizeof(float), 256); }
@@ -1007,8 +1065,10 @@ int pairs_for_device() {
 #ifdef MLA_TRACE
 extern "C" __attribute__((visibility("default"))) int mla_debug_read_trace(void *host,
                                                                           size_t bytes) {
-  if (bytes < sizeof(g_trace)) return -1;
-  return cudaMemcpyFromSymbol(host, g_trace, sizeof(g_trace)) == cudaSuccess ? 0 : -1;
+  if (bytes < sizeof(g_trace) + sizeof(g_trace_cta)) return -1;
+  if (cudaMemcpyFromSymbol(host, g_trace, sizeof(g_trace)) != cudaSuccess) return -1;
+  return cudaMemcpyFromSymbol(static_cast<char *>(host) + sizeof(g_trace), g_trace_cta,
+                              sizeof(g_trace_cta)) == cudaSuccess ? 0 : -1;
 }
 #endif
 
@@ -1029,14 +1089,9 @@ cudaError_t launch_decode_tc(const void *q_lat, const void *q_rope, const void *
   if ((long)B * Hq > kMaxItems) return cudaErrorNotSupported;
   char *ws = static_cast<char *>(workspace);
   float *o_part = reinterpret_cast<float *>(ws + kWsHeader);
-  const uint64_t rows = (uint64_t)B * Hq * d.H;
-  CUtensorMap tm_cache, tm_olat, tm_opart;
+  CUtensorMap tm_cache;
   if (!make_tmap_2d_bf16(&tm_cache, cache, kD, (uint64_t)num_blocks * kTile, kD * 2, 64, 64,
-                         CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_tmap_2d_bf16(&tm_olat, o_lat, kDc, rows, kDc * 2, 64, 32,
-                         CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_tmap_2d(&tm_opart, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, o_part, kDc,
-                    (uint64_t)2 * kMaxPairs * 128, kDc * 4, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B))
+                         CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1063,12 +1118,12 @@ cudaError_t launch_decode_tc(const void *q_lat, const void *q_rope, const void *
   a.o_part = o_part;
   a.lse_part = reinterpret_cast<float *>(ws + kWsHeader + part_bytes());
   a.plan = reinterpret_cast<int *>(ws + kWsHeader + part_bytes() + lse_part_bytes());
-  a.tma_olat = (d.H % 32) == 0;
-  decode_tc_kernel<<<2 * npairs, kThreads, kSmemBytes, st>>>(tm_cache, tm_olat, tm_opart, a);
+  decode_tc_kernel<<<2 * npairs, kThreads, kSmemBytes, st>>>(tm_cache, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  dim3 cgrid(B * Hq, (d.H + 15) / 16);
-  combine_tc_kernel<<<cgrid, 128, 0, st>>>(a);
+  const long rows_total = (long)B * Hq * d.H;
+  combine_tc_kernel<<<(unsigned)((rows_total + kCombineRows - 1) / kCombineRows),
+                      32 * kCombineRows, 0, st>>>(a);
   return cudaGetLastError();
 }
 
