@@ -81,12 +81,12 @@ constexpr uint16_t kMaskS = 1u << kRankS;
 // ---- shared memory (offsets from the 1024-aligned dynamic base)
 constexpr uint32_t kBox = 64 * 128;                // 64 rows x 128 B, 128B swizzle
 constexpr uint32_t kOffRing = 0;
-// S-CTA: [kStages] x (8 latent boxes + 1 RoPE box), query staging, the
-// published running maximum, one group's row statistics at a segment end
+// S-CTA: [kStages] x (8 latent boxes + 1 RoPE box), the published running
+// maximum, one group's row statistics at a segment end.  The ring also
+// carries each segment's query: two stages of 64 rows x [q_lat ; q_rope]
+// (exactly 2 x 72 KB) ahead of the segment's tiles.
 constexpr uint32_t kSStage = 9 * kBox;
-constexpr uint32_t kOffQStage = kStages * kSStage;  // 4 warps x 32 rows x 64 B
-constexpr uint32_t kQStageBytes = 4 * 2048;
-constexpr uint32_t kOffMDec = kOffQStage + kQStageBytes;  // m[128] f32
+constexpr uint32_t kOffMDec = kStages * kSStage;  // m[128] f32
 constexpr uint32_t kOffLM = kOffMDec + 128 * 4;           // m[128], l[128] f32
 constexpr uint32_t kSEnd = kOffLM + 2 * 128 * 4;
 // V-CTA: [kStages] x 8 latent boxes, P buffer per tile parity, their rescale
@@ -115,6 +115,7 @@ struct Bars {
   uint64_t sfull[6];                       // S: tile data landed
   uint64_t s_full[6], s_free[6];           // S: scores ready / read
   uint64_t q_full, q_free;                 // S: query in TMEM / QK^T of a segment done
+  uint64_t qfull[2];                       // S: query rows 64h..64h+63 landed in the ring
   uint64_t m_ready[2];                     // S: group i published its tile's maximum
   uint64_t seg_sync[2];                    // S: both softmax groups at a segment end
   uint64_t p_free[4];                      // S: V-CTA done with half h of P buffer i (2i+h)
@@ -163,9 +164,11 @@ struct DecodeArgs {
 // Developer tracing (built only with -DMLA_TRACE): %globaltimer stamps per
 // tile and role for two pairs (the first and the middle one), read back
 // with mla_debug_read_trace.  Events: 0 producer issued the tile's loads,
-// 1 MMA warp saw the tile's data, 2 S: QK^T issued / V: P arrived, 3 S:
-// softmax exponentials done / V: PV issued, 4 S: softmax saw S, 5 S: P buffer
-// free, 6 S: P sent, 7 per segment: S query loaded / V epilogue done.
+// 0 S: tile maximum agreed / V: producer issued the tile's loads, 1 MMA warp
+// saw the tile's data, 2 S: QK^T issued / V: first P half arrived, 3 S:
+// softmax exponentials done / V: PV issued, 4 S: softmax saw S / V: first
+// half's MMAs issued, 5 S: P buffer free, 6 S: P sent, 7 per segment: S query
+// loaded / V epilogue done.
 constexpr int kTraceTiles = 512, kTraceEvents = 8, kTracePairs = 2;
 __device__ unsigned long long g_trace[kTracePairs][2][kTraceEvents][kTraceTiles];
 // per CTA: kernel entry, range start (after setup), end of work
@@ -275,7 +278,9 @@ __device__ __forceinline__ void signal_abort(Misc *misc, uint32_t peer) {
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    decode_tc_kernel(const __grid_constant__ CUtensorMap tm_cache, DecodeArgs a) {
+    decode_tc_kernel(const __grid_constant__ CUtensorMap tm_cache,
+                     const __grid_constant__ CUtensorMap tm_qlat,
+                     const __grid_constant__ CUtensorMap tm_qrope, DecodeArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
   Bars *bars = reinterpret_cast<Bars *>(smem + kOffBars);
   Misc *misc = reinterpret_cast<Misc *>(smem + kOffMisc);
@@ -306,6 +311,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     ptx::mbar_init(&bars->q_full, 128);
     ptx::mbar_init(&bars->q_free, 2);
+    ptx::mbar_init(&bars->qfull[0], 1);
+    ptx::mbar_init(&bars->qfull[1], 1);
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(&bars->m_ready[s], 128);
       ptx::mbar_init(&bars->seg_sync[s], 256);
@@ -330,7 +337,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       ptx::mbar_arrive_expect_tx(&bars->stats_full, kStatsBytes);
     }
   }
-  if (warp == 0 && lane == 0) ptx::tma_prefetch_desc(&tm_cache);
+  if (warp == 0 && lane == 0) {
+    ptx::tma_prefetch_desc(&tm_cache);
+    if (isS) {
+      ptx::tma_prefetch_desc(&tm_qlat);
+      ptx::tma_prefetch_desc(&tm_qrope);
+    }
+  }
   if (warp == 1) ptx::tmem_alloc(&misc->tmem, 512);
   if (isS) {
     // tiles per item -> scan (scratch in the ring) -> this pair's range
@@ -414,25 +427,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     TableWindow cur;
     const uint32_t stage_bytes = isS ? kSStage : kVStage;
     const int nbox = isS ? 9 : 8;
+    int r = 0;  // ring position (tiles, plus two query stages per S segment)
     while (!failed && !*abort && it.next(&item, &lt0, &lt1, &whole, &n_vis)) {
       const int b = item / a.Hq;
       cur.reset(a.block_table + (size_t)b * a.max_blocks, lt1);
-      if (isS && lane == 0) {  // the query the softmax warps load next
-        const size_t row0 = (size_t)item * a.H;
-        const int nrows = a.H < 128 ? a.H : 128;
-        ptx::prefetch_l2(a.q_lat + row0 * kDc, (uint32_t)nrows * kDc * 2);
-        ptx::prefetch_l2(a.q_rope + row0 * kDr, (uint32_t)nrows * kDr * 2);
+      if (isS) {  // the segment's query: rows 0-63 and 64-127 of the item
+        for (int h = 0; h < 2; ++h, ++r) {
+          const int st = r % kStages;
+          if (r >= kStages && !wait_bar_warp(&bars->empty[st], ((r / kStages) - 1) & 1, abort)) {
+            failed = true;
+            break;
+          }
+          if (lane == 0) {
+            uint8_t *dst = smem + kOffRing + st * kSStage;
+            const int row0 = item * a.H + 64 * h;
+            ptx::mbar_arrive_expect_tx(&bars->qfull[h], 9 * kBox);
+            for (int k = 0; k < 8; ++k)
+              ptx::tma_load_2d(dst + k * kBox, &tm_qlat, &bars->qfull[h], k * 64, row0);
+            ptx::tma_load_2d(dst + 8 * kBox, &tm_qrope, &bars->qfull[h], 0, row0);
+          }
+        }
+        if (failed) break;
       }
-      for (int lt = lt0; lt < lt1; ++lt, ++g) {
-        const int st = g % kStages;
-        if (g >= kStages && !wait_bar_warp(&bars->empty[st], ((g / kStages) - 1) & 1, abort)) {
+      for (int lt = lt0; lt < lt1; ++lt, ++g, ++r) {
+        const int st = r % kStages;
+        if (r >= kStages && !wait_bar_warp(&bars->empty[st], ((r / kStages) - 1) & 1, abort)) {
           failed = true;
           break;
         }
         int blk = cur.at(lt, lane);
         if (blk < 0 || blk >= a.num_blocks) blk = 0;  // reported by the softmax warps
         if (lane == 0) {
-          MLA_TRACE_EV(0, g);
+          if (!isS) MLA_TRACE_EV(0, g);
           uint8_t *dst = smem + kOffRing + st * stage_bytes;
           uint64_t *fb = isS ? &bars->sfull[g % 6] : &bars->full[st];
           ptx::mbar_arrive_expect_tx(fb, nbox * kBox);
@@ -444,7 +470,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (failed) signal_abort(misc, peer);
     // leave only after this CTA's consumers released every stage it filled
     if (!*abort)
-      for (int k = g - kStages < 0 ? 0 : g - kStages; k < g; ++k)
+      for (int k = r - kStages < 0 ? 0 : r - kStages; k < r; ++k)
         wait_bar_warp(&bars->empty[k % kStages], (k / kStages) & 1, abort);
   } else if (isS && (warp == 1 || warp == 6)) {
     // ========== S-CTA: QK^T issuers (warp 1 even tiles, warp 6 odd tiles) ==========
@@ -454,14 +480,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint64_t ring_desc = ptx::smem_desc(ptx::smem_u32(smem + kOffRing), 16, 1024, ptx::kSw128);
       SegIter it;
       it.init(&a, W, t_begin, t_end, w0, s0);
-      int item, lt0, lt1, n_vis, seg = 0, g = 0;
+      int item, lt0, lt1, n_vis, seg = 0, g = 0, r = 0;
       bool whole, failed = false;
       while (!failed && it.next(&item, &lt0, &lt1, &whole, &n_vis)) {
         if (!wait_bar(&bars->q_full, seg & 1, abort)) { failed = true; break; }
         ptx::tc_fence_after();
-        for (int lt = lt0; lt < lt1; ++lt, ++g) {
+        r += 2;  // the segment's query stages
+        for (int lt = lt0; lt < lt1; ++lt, ++g, ++r) {
           if ((g & 1) != mine) continue;
-          const int st = g % kStages, sb = g % 3;
+          const int st = r % kStages, sb = g % 3;
           if (!wait_bar(&bars->sfull[g % 6], (g / 6) & 1, abort)) { failed = true; break; }
           MLA_TRACE_EV(1, g);
           // score buffer sb was last read by the softmax of tile g-3
@@ -548,6 +575,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
             // the last tile's P buffer becomes the epilogue's staging
             if (lt != lt1 - 1) ptx::mma_commit_mc(&bars->p_free[2 * pb + half], kMaskS);
+            if (half == 0) MLA_TRACE_EV(4, g);
           }
           if (failed) break;
           ptx::mma_commit(&bars->empty[st]);
@@ -576,7 +604,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int row = 32 * wq + lane;
     const uint32_t lane_base = (uint32_t)(32 * wq) << 16;
     const int gtid = threadIdx.x - (grp ? 224 : 64);  // 0..127 within the group
-    uint8_t *qst = smem + kOffQStage + wq * 2048;     // 32 rows x 64 B
     float *m_dec = reinterpret_cast<float *>(smem + kOffMDec);
     float *lm = reinterpret_cast<float *>(smem + kOffLM);
     const uint32_t rP = ptx::map_to_rank(smem + kOffP + grp * kPBytes, kRankV);
@@ -589,7 +616,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     (void)gtid;
     SegIter it;
     it.init(&a, W, t_begin, t_end, w0, s0);
-    int item, lt0, lt1, n_vis, seg = 0, g = 0;
+    int item, lt0, lt1, n_vis, seg = 0, g = 0, r_pos = 0;
     bool whole, failed = false;
     // both softmax groups meet twice per segment end (bounded waits, one
     // phase per segment on each barrier)
@@ -611,59 +638,56 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         seg_bad = __any_sync(0xffffffffu, bad);
       }
-      // -- this item's query -> TMEM (loaded by the group owning the first
-      //    tile), once the previous segment's QK^T no longer reads it --
+      // -- this item's query -> TMEM: the producer put its 128 rows in the
+      //    two ring stages before the segment's tiles; the group owning the
+      //    first tile copies them once the previous segment's QK^T is done,
+      //    then hands the stages back --
+      const int rq = r_pos;
+      r_pos += 2 + (lt1 - lt0);
       if (seg > 0 && !wait_bar_warp(&bars->q_free, (seg - 1) & 1, abort)) { failed = true; break; }
       if ((g_first & 1) == grp) {
+        // only the owner waits: the next query cannot land before this one's
+        // stages are returned below, so it is never two phases behind
+        if (!wait_bar_warp(&bars->qfull[0], seg & 1, abort) ||
+            !wait_bar_warp(&bars->qfull[1], seg & 1, abort)) {
+          failed = true;
+          break;
+        }
         ptx::tc_fence_after();
-        const size_t row0 = (size_t)item * a.H + 32 * wq;
-        const int nvalid = a.H - 32 * wq;  // rows of this warp that exist
-        // coalesced loads (4 lanes per 64-byte piece of a row), transposed
-        // through shared memory to one row per lane
-        auto load_chunk = [&](int chunk, uint4 (&v)[4]) {
+        const bool real = row < a.H;  // rows past the heads read as zero
+        // row = lane of this thread: stage (rq + row/64), box k holds columns
+        // 64k..64k+63 as 128-byte rows, 16-byte chunk c at (c ^ row%8)
+        const uint8_t *qrow = smem + kOffRing + ((rq + (row >> 6)) % kStages) * kSStage +
+                              (row & 63) * 128;
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int r = 8 * i + (lane >> 2), part = lane & 3;
-            v[i] = make_uint4(0, 0, 0, 0);
-            if (r < nvalid) {
-              const uint4 *src = chunk < 16
-                  ? reinterpret_cast<const uint4 *>(a.q_lat + (row0 + r) * kDc + chunk * 32)
-                  : reinterpret_cast<const uint4 *>(a.q_rope + (row0 + r) * kDr + (chunk - 16) * 32);
-              v[i] = __ldg(src + part);
-            }
-          }
-        };
-        // three rounds of 6 chunks, all of a round's loads in flight at once
+        for (int k = 0; k < 9; ++k) {
 #pragma unroll
-        for (int rd = 0; rd < 3; ++rd) {
-          uint4 cur[6][4];
-#pragma unroll
-          for (int j = 0; j < 6; ++j) load_chunk(6 * rd + j, cur[j]);
-#pragma unroll
-          for (int j = 0; j < 6; ++j) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int r = 8 * i + (lane >> 2), part = lane & 3;
-              *reinterpret_cast<uint4 *>(qst + r * 64 + ((part ^ ((r >> 1) & 3)) << 4)) = cur[j][i];
-            }
-            __syncwarp();
+          for (int hh = 0; hh < 2; ++hh) {
             uint32_t v[16];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const uint4 x = *reinterpret_cast<const uint4 *>(qst + lane * 64 + ((k ^ ((lane >> 1) & 3)) << 4));
-              v[4 * k] = x.x;
-              v[4 * k + 1] = x.y;
-              v[4 * k + 2] = x.z;
-              v[4 * k + 3] = x.w;
+            for (int c2 = 0; c2 < 4; ++c2) {
+              const int c = 4 * hh + c2;
+              uint4 x = *reinterpret_cast<const uint4 *>(qrow + k * kBox + ((c ^ (row & 7)) << 4));
+              if (!real) x = make_uint4(0, 0, 0, 0);
+              v[4 * c2] = x.x;
+              v[4 * c2 + 1] = x.y;
+              v[4 * c2 + 2] = x.z;
+              v[4 * c2 + 3] = x.w;
             }
-            ptx::tmem_st16_nc(tmem + lane_base + kTmemQ + (6 * rd + j) * 16, v);
-            __syncwarp();
+            ptx::tmem_st16_nc(tmem + lane_base + kTmemQ + k * 32 + hh * 16, v);
           }
         }
         ptx::tmem_st_wait();
         ptx::tc_fence_before();
         ptx::mbar_arrive(&bars->q_full);
         if (lane == 0 && wq == 0) MLA_TRACE_EV(7, seg);
+        // every row is copied once q_full completes: the stages go back
+        if (threadIdx.x == (grp ? 224 : 64)) {
+          if (wait_bar(&bars->q_full, seg & 1, abort)) {
+            ptx::mbar_arrive(&bars->empty[rq % kStages]);
+            ptx::mbar_arrive(&bars->empty[(rq + 1) % kStages]);
+          }
+        }
       }
 
       // this group's row sum over its tiles of the segment, relative to m_mine
@@ -750,6 +774,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         m_dec[row] = m_use;
         ptx::mbar_arrive(&bars->m_ready[grp]);
+        if (lane == 0 && wq == 0) MLA_TRACE_EV(0, g);
         if (!send_prev()) { failed = true; break; }
         float lsum = 0.f;
 #pragma unroll
@@ -1089,8 +1114,13 @@ cudaError_t launch_decode_tc(const void *q_lat, const void *q_rope, const void *
   if ((long)B * Hq > kMaxItems) return cudaErrorNotSupported;
   char *ws = static_cast<char *>(workspace);
   float *o_part = reinterpret_cast<float *>(ws + kWsHeader);
-  CUtensorMap tm_cache;
+  const uint64_t rows = (uint64_t)B * Hq * d.H;
+  CUtensorMap tm_cache, tm_qlat, tm_qrope;
   if (!make_tmap_2d_bf16(&tm_cache, cache, kD, (uint64_t)num_blocks * kTile, kD * 2, 64, 64,
+                         CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap_2d_bf16(&tm_qlat, q_lat, kDc, rows, kDc * 2, 64, 64,
+                         CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap_2d_bf16(&tm_qrope, q_rope, kDr, rows, kDr * 2, 64, 64,
                          CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel,
@@ -1118,7 +1148,7 @@ cudaError_t launch_decode_tc(const void *q_lat, const void *q_rope, const void *
   a.o_part = o_part;
   a.lse_part = reinterpret_cast<float *>(ws + kWsHeader + part_bytes());
   a.plan = reinterpret_cast<int *>(ws + kWsHeader + part_bytes() + lse_part_bytes());
-  decode_tc_kernel<<<2 * npairs, kThreads, kSmemBytes, st>>>(tm_cache, a);
+  decode_tc_kernel<<<2 * npairs, kThreads, kSmemBytes, st>>>(tm_cache, tm_qlat, tm_qrope, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const long rows_total = (long)B * Hq * d.H;

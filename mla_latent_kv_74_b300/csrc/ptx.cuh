@@ -86,16 +86,31 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t pa
   return ok != 0;
 }
 
+// Non-suspending probe, cluster-scope acquire.  Waits on barriers that
+// another CTA of the cluster arrives on poll with this instead of try_wait:
+// a thread suspended in try_wait can be woken late by a remote arrival.
+__device__ __forceinline__ bool mbar_test_wait_cluster(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n"
+      " mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait for the phase with the given parity to complete.  Gives up
 // (returns false) after kWaitLimitNs, or earlier once *abort becomes nonzero.
 template <bool kClusterScope = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
                                           const volatile int *abort = nullptr) {
-  if (kClusterScope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity))
+  if (kClusterScope ? mbar_test_wait_cluster(bar, parity) : mbar_try_wait(bar, parity))
     return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
-    if (kClusterScope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity))
+    if (kClusterScope ? mbar_test_wait_cluster(bar, parity) : mbar_try_wait(bar, parity))
       return true;
     if ((i & 63) == 0) {
       if (abort && *abort) return false;
