@@ -302,11 +302,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     misc->bad_smem = (ptx::smem_u32(smem) & 1023u) != 0;
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(&bars->full[s], 1);
-      ptx::mbar_init(&bars->empty[s], 1);
+      ptx::mbar_init(&bars->empty[s], isS ? 2 : 1);  // S: both QK^T issuers read a stage
     }
     for (int s = 0; s < 6; ++s) {
       ptx::mbar_init(&bars->sfull[s], 1);
-      ptx::mbar_init(&bars->s_full[s], 1);
+      ptx::mbar_init(&bars->s_full[s], 2);
       ptx::mbar_init(&bars->s_free[s], 128);
     }
     ptx::mbar_init(&bars->q_full, 128);
@@ -473,7 +473,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int k = r - kStages < 0 ? 0 : r - kStages; k < r; ++k)
         wait_bar_warp(&bars->empty[k % kStages], (k / kStages) & 1, abort);
   } else if (isS && (warp == 1 || warp == 6)) {
-    // ========== S-CTA: QK^T issuers (warp 1 even tiles, warp 6 odd tiles) ==========
+    // ========== S-CTA: QK^T issuers ==========
+    // Both issue every tile, each half of its 36 k-steps into its own partial
+    // score buffer (warp 1: latent boxes 0-3 and half of box 4, warp 6: the
+    // rest and the RoPE box); the softmax adds the two.  One thread alone
+    // cannot issue N=64 MMAs at the tensor pipe's rate, two can.
     if (lane == 0) {
       const int mine = warp == 1 ? 0 : 1;
       const uint32_t idesc = ptx::idesc_bf16(128, kTile, false, false);
@@ -487,23 +491,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         ptx::tc_fence_after();
         r += 2;  // the segment's query stages
         for (int lt = lt0; lt < lt1; ++lt, ++g, ++r) {
-          if ((g & 1) != mine) continue;
-          const int st = r % kStages, sb = g % 3;
+          const int st = r % kStages, sb = (2 * g + mine) % 3;
           if (!wait_bar(&bars->sfull[g % 6], (g / 6) & 1, abort)) { failed = true; break; }
-          MLA_TRACE_EV(1, g);
-          // score buffer sb was last read by the softmax of tile g-3
-          if (g >= 3 && !wait_bar(&bars->s_free[(g - 3) % 6], ((g - 3) / 6) & 1, abort)) { failed = true; break; }
+          if (mine == (g & 1)) MLA_TRACE_EV(1, g);
+          // partial buffer sb last held partial 2g+mine-3: tile g-2's second
+          // (for warp 1) or tile g-1's first (for warp 6)
+          const int gp = g - 2 + mine;
+          if (gp >= 0 && !wait_bar(&bars->s_free[gp % 6], (gp / 6) & 1, abort)) { failed = true; break; }
           ptx::tc_fence_after();
           const uint32_t d = tmem + kTmemS + sb * kTile;
           const uint64_t bs = ring_desc + (uint64_t)((st * kSStage) >> 4);
 #pragma unroll
-          for (int kk = 0; kk < 36; ++kk)  // 9 boxes (8 latent + RoPE) x 4 k-steps of 16
+          for (int j = 0; j < 18; ++j) {  // 9 boxes (8 latent + RoPE) x 4 k-steps of 16
+            const int kk = 18 * mine + j;
             ptx::mma_bf16_ts(d, tmem + kTmemQ + kk * 8,
                              bs + (uint64_t)((((kk >> 2) * kBox) + (kk & 3) * 32) >> 4), idesc,
-                             kk != 0);
+                             j != 0);
+          }
           ptx::mma_commit(&bars->s_full[g % 6]);
           ptx::mma_commit(&bars->empty[st]);
-          MLA_TRACE_EV(2, g);
+          if (mine == (g & 1)) MLA_TRACE_EV(2, g);
         }
         if (failed) break;
         ptx::mma_commit(&bars->q_free);
@@ -684,8 +691,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // every row is copied once q_full completes: the stages go back
         if (threadIdx.x == (grp ? 224 : 64)) {
           if (wait_bar(&bars->q_full, seg & 1, abort)) {
-            ptx::mbar_arrive(&bars->empty[rq % kStages]);
-            ptx::mbar_arrive(&bars->empty[(rq + 1) % kStages]);
+            for (int i = 0; i < 2; ++i) {  // stands for both issuers' releases
+              ptx::mbar_arrive(&bars->empty[rq % kStages]);
+              ptx::mbar_arrive(&bars->empty[(rq + 1) % kStages]);
+            }
           }
         }
       }
@@ -734,7 +743,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       };
       for (int lt = lt0; lt < lt1; ++lt, ++g) {
         if ((g & 1) != grp) continue;
-        const int sb = g % 3;
+        const int sb0 = (2 * g) % 3, sb1 = (2 * g + 1) % 3;
         if (!wait_bar_warp(&bars->s_full[g % 6], (g / 6) & 1, abort)) { failed = true; break; }
         if (lane == 0 && wq == 0) MLA_TRACE_EV(4, g);
         ptx::tc_fence_after();
@@ -742,11 +751,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           float v[16];
-          ptx::tmem_ld16(tmem + lane_base + kTmemS + sb * kTile + q * 16, v);
+          ptx::tmem_ld16(tmem + lane_base + kTmemS + sb0 * kTile + q * 16, v);
 #pragma unroll
           for (int i = 0; i < 16; ++i) s[q * 16 + i] = v[i];
         }
         ptx::tmem_ld_wait();
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {  // the second partial, 32 columns at a time
+          float v[2][16];
+#pragma unroll
+          for (int q = 0; q < 2; ++q)
+            ptx::tmem_ld16(tmem + lane_base + kTmemS + sb1 * kTile + (2 * h2 + q) * 16, v[q]);
+          ptx::tmem_ld_wait();
+#pragma unroll
+          for (int q = 0; q < 2; ++q)
+#pragma unroll
+            for (int i = 0; i < 16; ++i) s[(2 * h2 + q) * 16 + i] += v[q][i];
+        }
         ptx::tc_fence_before();
         ptx::mbar_arrive(&bars->s_free[g % 6]);
         const int tok0 = lt * kTile;
