@@ -345,6 +345,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
   }
   if (warp == 1) ptx::tmem_alloc(&misc->tmem, 512);
+  // Launched as a programmatic dependent: everything above overlaps the tail
+  // of the previous kernel in the stream; its outputs (queries, and possibly
+  // lengths or the cache) are read only after this wait.  Every CTA of this
+  // grid is resident once all pass here, so the combine kernel may launch.
+  ptx::grid_dependency_wait();
+  ptx::launch_dependents();
   if (isS) {
     // tiles per item -> scan (scratch in the ring) -> this pair's range
     int *pre = reinterpret_cast<int *>(smem + kOffRing);
@@ -1008,6 +1014,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 // directly by their pair return at once.
 constexpr int kCombineRows = 8;
 __global__ void __launch_bounds__(32 * kCombineRows) combine_tc_kernel(DecodeArgs a) {
+  // launched early, behind the decode grid: its pieces are complete and
+  // visible only after this wait
+  ptx::grid_dependency_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long rowg = (long)blockIdx.x * kCombineRows + warp;
   const int W = a.B * a.Hq;
@@ -1169,13 +1178,25 @@ cudaError_t launch_decode_tc(const void *q_lat, const void *q_rope, const void *
   a.o_part = o_part;
   a.lse_part = reinterpret_cast<float *>(ws + kWsHeader + part_bytes());
   a.plan = reinterpret_cast<int *>(ws + kWsHeader + part_bytes() + lse_part_bytes());
-  decode_tc_kernel<<<2 * npairs, kThreads, kSmemBytes, st>>>(tm_cache, tm_qlat, tm_qrope, a);
-  e = cudaGetLastError();
+  // both kernels are programmatic dependents of their predecessor in the
+  // stream (each waits on it in-kernel before reading its outputs)
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * npairs, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = st;
+  cfg.attrs = pdl;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, decode_tc_kernel, tm_cache, tm_qlat, tm_qrope, a);
   if (e != cudaSuccess) return e;
   const long rows_total = (long)B * Hq * d.H;
-  combine_tc_kernel<<<(unsigned)((rows_total + kCombineRows - 1) / kCombineRows),
-                      32 * kCombineRows, 0, st>>>(a);
-  return cudaGetLastError();
+  cfg.gridDim = dim3((unsigned)((rows_total + kCombineRows - 1) / kCombineRows), 1, 1);
+  cfg.blockDim = dim3(32 * kCombineRows, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  return cudaLaunchKernelEx(&cfg, combine_tc_kernel, a);
 }
 
 }  // namespace mla

@@ -119,6 +119,20 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
   }
 }
 
+// ---- programmatic dependent launch -------------------------------------------------
+
+// Blocks until the previous grid in the stream has completed and its memory
+// operations are visible (returns at once when launched without the
+// programmatic-serialization attribute).
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Allows the next grid in the stream (if launched as a programmatic
+// dependent) to be scheduled once every CTA of this grid has signalled.
+__device__ __forceinline__ void launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- TMA ------------------------------------------------------------------------
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
