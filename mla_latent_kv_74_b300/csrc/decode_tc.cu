@@ -113,7 +113,8 @@ struct Bars {
   // S: per tile g, barrier g % 6 (stage g % 3, issuer and softmax group
   // g % 2), so each barrier has one waiter that never falls a phase behind
   uint64_t sfull[6];                       // S: tile data landed
-  uint64_t s_full[6], s_free[6];           // S: scores ready / read
+  // S: partial scores of tile g from issuer h ready / read: index 2*(g%6)+h
+  uint64_t s_full[12], s_free[12];
   uint64_t q_full, q_free;                 // S: query in TMEM / QK^T of a segment done
   uint64_t qfull[2];                       // S: query rows 64h..64h+63 landed in the ring
   uint64_t m_ready[2];                     // S: group i published its tile's maximum
@@ -304,11 +305,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       ptx::mbar_init(&bars->full[s], 1);
       ptx::mbar_init(&bars->empty[s], isS ? 2 : 1);  // S: both QK^T issuers read a stage
     }
-    for (int s = 0; s < 6; ++s) {
-      ptx::mbar_init(&bars->sfull[s], 1);
-      ptx::mbar_init(&bars->s_full[s], 2);
+    for (int s = 0; s < 12; ++s) {
+      ptx::mbar_init(&bars->s_full[s], 1);
       ptx::mbar_init(&bars->s_free[s], 128);
     }
+    for (int s = 0; s < 6; ++s) ptx::mbar_init(&bars->sfull[s], 1);
     ptx::mbar_init(&bars->q_full, 128);
     ptx::mbar_init(&bars->q_free, 2);
     ptx::mbar_init(&bars->qfull[0], 1);
@@ -501,9 +502,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (!wait_bar(&bars->sfull[g % 6], (g / 6) & 1, abort)) { failed = true; break; }
           if (mine == (g & 1)) MLA_TRACE_EV(1, g);
           // partial buffer sb last held partial 2g+mine-3: tile g-2's second
-          // (for warp 1) or tile g-1's first (for warp 6)
+          // (for warp 1) or tile g-1's first (for warp 6), released as soon
+          // as the softmax has read that one partial
           const int gp = g - 2 + mine;
-          if (gp >= 0 && !wait_bar(&bars->s_free[gp % 6], (gp / 6) & 1, abort)) { failed = true; break; }
+          if (gp >= 0 && !wait_bar(&bars->s_free[2 * (gp % 6) + (1 - mine)], (gp / 6) & 1, abort)) {
+            failed = true;
+            break;
+          }
           ptx::tc_fence_after();
           const uint32_t d = tmem + kTmemS + sb * kTile;
           const uint64_t bs = ring_desc + (uint64_t)((st * kSStage) >> 4);
@@ -514,7 +519,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                              bs + (uint64_t)((((kk >> 2) * kBox) + (kk & 3) * 32) >> 4), idesc,
                              j != 0);
           }
-          ptx::mma_commit(&bars->s_full[g % 6]);
+          ptx::mma_commit(&bars->s_full[2 * (g % 6) + mine]);
           ptx::mma_commit(&bars->empty[st]);
           if (mine == (g & 1)) MLA_TRACE_EV(2, g);
         }
@@ -714,13 +719,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       float alpha_prev = 1.f;
       bool resc_prev = false;
       int g_prev = -1;
-      auto send_prev = [&]() -> bool {
+      // The previous tile's P leaves in two halves, each followed by half of
+      // this tile's exponentials, so the transfer overlaps the arithmetic.
+      auto send_half = [&](int half) -> bool {
         if (g_prev < 0) return true;
         const uint32_t prow = rP + row * 128;
         const int ph = ((g_prev >> 1) - 1) & 1;
-        // half 0 (tokens 0-31) with the rescale factors and flags; each half
-        // of buffer grp was last read by the V-CTA's PV of tile g_prev-2
-        if (g_prev >= 2 && !wait_bar_warp(&bars->p_free[2 * grp], ph, abort, true)) return false;
+        // each half of buffer grp was last read by the V-CTA's PV of tile g_prev-2
+        if (g_prev >= 2 && !wait_bar_warp(&bars->p_free[2 * grp + half], ph, abort, true)) return false;
+        if (half == 1) {  // tokens 32-63
+#pragma unroll
+          for (int cc = 4; cc < 8; ++cc)
+            ptx::st_async_v4(prow + ((cc ^ (lane & 7)) << 4), pk_prev[4 * cc], pk_prev[4 * cc + 1],
+                             pk_prev[4 * cc + 2], pk_prev[4 * cc + 3], rPFullB);
+          if (lane == 0 && wq == 0) MLA_TRACE_EV(6, g_prev);
+          g_prev = -1;
+          return true;
+        }
+        // half 0 (tokens 0-31) with the rescale factors and flags
         if (lane == 0 && wq == 0) MLA_TRACE_EV(5, g_prev);
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc)
@@ -737,20 +753,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         const uint32_t wflag = __ballot_sync(0xffffffffu, resc_prev);
         if (lane == 0) ptx::st_async_b32(rAux + 512 + wq * 4, wflag, rPFullA);
-        // half 1 (tokens 32-63)
-        if (g_prev >= 2 && !wait_bar_warp(&bars->p_free[2 * grp + 1], ph, abort, true)) return false;
-#pragma unroll
-        for (int cc = 4; cc < 8; ++cc)
-          ptx::st_async_v4(prow + ((cc ^ (lane & 7)) << 4), pk_prev[4 * cc], pk_prev[4 * cc + 1],
-                           pk_prev[4 * cc + 2], pk_prev[4 * cc + 3], rPFullB);
-        if (lane == 0 && wq == 0) MLA_TRACE_EV(6, g_prev);
-        g_prev = -1;
         return true;
       };
+      auto send_prev = [&]() -> bool { return send_half(0) && send_half(1); };
       for (int lt = lt0; lt < lt1; ++lt, ++g) {
         if ((g & 1) != grp) continue;
         const int sb0 = (2 * g) % 3, sb1 = (2 * g + 1) % 3;
-        if (!wait_bar_warp(&bars->s_full[g % 6], (g / 6) & 1, abort)) { failed = true; break; }
+        // the first partial is read (and its buffer handed back to the
+        // second issuer's next tile) before the second is waited for
+        if (!wait_bar_warp(&bars->s_full[2 * (g % 6)], (g / 6) & 1, abort)) { failed = true; break; }
         if (lane == 0 && wq == 0) MLA_TRACE_EV(4, g);
         ptx::tc_fence_after();
         float s[64];
@@ -762,6 +773,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 16; ++i) s[q * 16 + i] = v[i];
         }
         ptx::tmem_ld_wait();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(&bars->s_free[2 * (g % 6)]);
+        if (!wait_bar_warp(&bars->s_full[2 * (g % 6) + 1], (g / 6) & 1, abort)) { failed = true; break; }
+        ptx::tc_fence_after();
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2) {  // the second partial, 32 columns at a time
           float v[2][16];
@@ -775,17 +790,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 16; ++i) s[(2 * h2 + q) * 16 + i] += v[q][i];
         }
         ptx::tc_fence_before();
-        ptx::mbar_arrive(&bars->s_free[g % 6]);
+        ptx::mbar_arrive(&bars->s_free[2 * (g % 6) + 1]);
         const int tok0 = lt * kTile;
         if (tok0 + kTile > n_vis) {
 #pragma unroll
           for (int j = 0; j < 64; ++j)
             if (tok0 + j >= n_vis) s[j] = -INFINITY;
         }
-        float mx = s[0];
+        float mx4[4] = {s[0], s[1], s[2], s[3]};
 #pragma unroll
-        for (int j = 1; j < 64; ++j) mx = fmaxf(mx, s[j]);
-        const float mt = mx * c;
+        for (int j = 4; j < 64; ++j) mx4[j & 3] = fmaxf(mx4[j & 3], s[j]);
+        const float mt = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * c;
         // the previous tile's maximum (published by the other group)
         if (g > 0 && !wait_bar_warp(&bars->m_ready[grp ^ 1], ((g - 1) >> 1) & 1, abort)) { failed = true; break; }
         float m_use = mt, alpha = 1.f;
@@ -802,15 +817,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         m_dec[row] = m_use;
         ptx::mbar_arrive(&bars->m_ready[grp]);
         if (lane == 0 && wq == 0) MLA_TRACE_EV(0, g);
-        if (!send_prev()) { failed = true; break; }
-        float lsum = 0.f;
+        float ls[2] = {0.f, 0.f};
+        bool sent = true;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float p0 = ptx::ex2(fmaf(s[2 * i], c, -m_use));
-          const float p1 = ptx::ex2(fmaf(s[2 * i + 1], c, -m_use));
-          lsum += p0 + p1;
-          pk_prev[i] = ptx::pack_bf16x2(p0, p1);
+        for (int half = 0; half < 2; ++half) {
+          sent = sent && send_half(half);  // frees pk_prev[16*half ..]
+#pragma unroll
+          for (int i = 16 * half; i < 16 * half + 16; ++i) {
+            const float p0 = ptx::ex2(fmaf(s[2 * i], c, -m_use));
+            const float p1 = ptx::ex2(fmaf(s[2 * i + 1], c, -m_use));
+            ls[i & 1] += p0 + p1;
+            pk_prev[i] = ptx::pack_bf16x2(p0, p1);
+          }
         }
+        if (!sent) { failed = true; break; }
+        const float lsum = ls[0] + ls[1];
         alpha_prev = alpha;
         resc_prev = resc;
         g_prev = g;
