@@ -280,6 +280,7 @@ __device__ __forceinline__ void signal_abort(Misc *misc, uint32_t peer) {
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tm_cache,
+                     const __grid_constant__ CUtensorMap tm_cache_v,
                      const __grid_constant__ CUtensorMap tm_qlat,
                      const __grid_constant__ CUtensorMap tm_qrope, DecodeArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -339,7 +340,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
   }
   if (warp == 0 && lane == 0) {
-    ptx::tma_prefetch_desc(&tm_cache);
+    ptx::tma_prefetch_desc(isS ? &tm_cache : &tm_cache_v);
     if (isS) {
       ptx::tma_prefetch_desc(&tm_qlat);
       ptx::tma_prefetch_desc(&tm_qrope);
@@ -449,8 +450,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             uint8_t *dst = smem + kOffRing + st * kSStage;
             const int row0 = item * a.H + 64 * h;
             ptx::mbar_arrive_expect_tx(&bars->qfull[h], 9 * kBox);
-            for (int k = 0; k < 8; ++k)
-              ptx::tma_load_2d(dst + k * kBox, &tm_qlat, &bars->qfull[h], k * 64, row0);
+            ptx::tma_load_3d(dst, &tm_qlat, &bars->qfull[h], 0, row0, 0);  // 8 latent boxes
             ptx::tma_load_2d(dst + 8 * kBox, &tm_qrope, &bars->qfull[h], 0, row0);
           }
         }
@@ -468,9 +468,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (!isS) MLA_TRACE_EV(0, g);
           uint8_t *dst = smem + kOffRing + st * stage_bytes;
           uint64_t *fb = isS ? &bars->sfull[g % 6] : &bars->full[st];
+          // the whole stage in one copy: nbox boxes of 64 rows x 128 B
           ptx::mbar_arrive_expect_tx(fb, nbox * kBox);
-          for (int k = 0; k < nbox; ++k)
-            ptx::tma_load_2d(dst + k * kBox, &tm_cache, fb, k * 64, blk * kTile);
+          ptx::tma_load_3d(dst, isS ? &tm_cache : &tm_cache_v, fb, 0, blk * kTile, 0);
         }
       }
     }
@@ -1166,11 +1166,17 @@ cudaError_t launch_decode_tc(const void *q_lat, const void *q_rope, const void *
   char *ws = static_cast<char *>(workspace);
   float *o_part = reinterpret_cast<float *>(ws + kWsHeader);
   const uint64_t rows = (uint64_t)B * Hq * d.H;
-  CUtensorMap tm_cache, tm_qlat, tm_qrope;
-  if (!make_tmap_2d_bf16(&tm_cache, cache, kD, (uint64_t)num_blocks * kTile, kD * 2, 64, 64,
-                         CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_tmap_2d_bf16(&tm_qlat, q_lat, kDc, rows, kDc * 2, 64, 64,
-                         CU_TENSOR_MAP_SWIZZLE_128B) ||
+  // The cache and q_lat as [column block of 64][row][64]: one copy moves a
+  // whole stage, box k of it (columns 64k..64k+63) 8 KB after box k-1, each
+  // box 64 rows x 128 B in the 128-byte swizzle.
+  CUtensorMap tm_cache, tm_cache_v, tm_qlat, tm_qrope;
+  const uint64_t cache_rows = (uint64_t)num_blocks * kTile;
+  if (!make_tmap_3d(&tm_cache, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cache, 64, cache_rows, kD / 64,
+                    kD * 2, 128, 64, 64, kD / 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap_3d(&tm_cache_v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cache, 64, cache_rows, kD / 64,
+                    kD * 2, 128, 64, 64, kDc / 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap_3d(&tm_qlat, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, q_lat, 64, rows, kDc / 64,
+                    kDc * 2, 128, 64, 64, kDc / 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_tmap_2d_bf16(&tm_qrope, q_rope, kDr, rows, kDr * 2, 64, 64,
                          CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
@@ -1211,7 +1217,7 @@ cudaError_t launch_decode_tc(const void *q_lat, const void *q_rope, const void *
   cfg.stream = st;
   cfg.attrs = pdl;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, decode_tc_kernel, tm_cache, tm_qlat, tm_qrope, a);
+  e = cudaLaunchKernelEx(&cfg, decode_tc_kernel, tm_cache, tm_cache_v, tm_qlat, tm_qrope, a);
   if (e != cudaSuccess) return e;
   const long rows_total = (long)B * Hq * d.H;
   cfg.gridDim = dim3((unsigned)((rows_total + kCombineRows - 1) / kCombineRows), 1, 1);

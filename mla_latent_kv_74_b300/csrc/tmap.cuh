@@ -42,6 +42,24 @@ inline bool make_tmap_2d(CUtensorMap *map, CUtensorMapDataType type, const void 
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// A 3-D view [d2][d1][d0] with arbitrary byte strides for d1 and d2 (they
+// need not grow with the dimension), moved in boxes of box0 x box1 x box2;
+// a box lands in shared memory with d0 fastest, then d1, then d2.
+inline bool make_tmap_3d(CUtensorMap *map, CUtensorMapDataType type, const void *base,
+                         uint64_t d0, uint64_t d1, uint64_t d2, uint64_t stride1,
+                         uint64_t stride2, uint32_t box0, uint32_t box1, uint32_t box2,
+                         CUtensorMapSwizzle swizzle) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {stride1, stride2};
+  cuuint32_t box[3] = {box0, box1, box2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, type, 3, const_cast<void *>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 inline bool make_tmap_2d_bf16(CUtensorMap *map, const void *base, uint64_t inner, uint64_t outer,
                               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
                               CUtensorMapSwizzle swizzle) {
