@@ -200,6 +200,10 @@ def run_ours(args, rank, world, device):
     torch.cuda.synchronize()
     with ClockSampler(smi_index(device.index)) as clocks:
         t_wall = time.perf_counter()
+        # A spin kernel ahead of the timed steps (outside every event pair)
+        # gives the host time to enqueue them all, so no measured interval
+        # contains the GPU waiting for the next launch (about 1 ms per step).
+        torch.cuda._sleep(int(min(2e9, 2e6 * args.steps)))
         for it in range(args.steps):
             ev = evs[it]
             flush.zero_()
