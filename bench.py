@@ -242,6 +242,9 @@ def run_ours(args, rank, world, device):
         if it >= args.warmup:
             e2e_ms.append(e0.elapsed_time(e1))
 
+    # ---- the fused projection-and-append step (measured on its own) ---------
+    proj = measure_project_append(mla, args, w, dev, inp, dims, flush, stream, device)
+
     # ---- reduce over ranks ----------------------------------------------------
     t_step = float(np.mean(step_ms))
     t_dec = float(np.mean(dec_ms))
@@ -325,7 +328,66 @@ def run_ours(args, rank, world, device):
         "clocks": clocks.summary(),
         "wall_s_timed_region": round(t_wall, 3),
     }
+    if proj is not None:
+        res["project_append"] = proj
     return res
+
+
+# hidden size of the model each workload is shaped after (DeepSeek-V2: 5120,
+# V2-Lite: 2048), for the fused projection-and-append measurement
+PROJ_D_MODEL = {"v2": 5120, "mtp": 5120, "long": 5120, "lite": 2048}
+
+
+def measure_project_append(mla, args, w, dev, inp, dims, flush, stream, device):
+    """``mla_project_append`` for the step's new tokens (B * Hq of them) at the
+    model's hidden size: CUDA events around each call, L2 flushed before it,
+    all calls enqueued behind a spin kernel.  The algorithmic bytes are the
+    two weights, the hidden states and the cache rows written; the FLOPs
+    ``2 * tokens * (d_c + d_r) * d_model``."""
+    d_model = PROJ_D_MODEL.get(w.name)
+    if d_model is None or w.dtype != "bf16":
+        return None
+    T = w.B * w.Hq
+    pt = {k: v.to(device) for k, v in synth.project_tensors(w.seed + 100, w.B, w.Hq, d_model,
+                                                            w.d_c, w.d_r).items()}
+    ws = torch.empty(mla.mla_project_append_workspace_size(w.B, w.Hq, d_model, dims),
+                     dtype=torch.uint8, device=device)
+
+    def call():
+        mla.mla_project_append(pt["h"], pt["W_DKV"], pt["W_KR"], dev["cache"],
+                               inp["num_blocks"], dev["block_table"], dev["seqlens"], dims, ws,
+                               stream=stream)
+
+    for _ in range(3):
+        flush.zero_()
+        call()
+    n = max(3, min(args.steps, 50))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n)]
+    torch.cuda.synchronize()
+    torch.cuda._sleep(int(2e6 * n))
+    for e0, e1 in evs:
+        flush.zero_()
+        e0.record(stream)
+        call()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms = float(np.mean([e0.elapsed_time(e1) for e0, e1 in evs]))
+    D = w.d_c + w.d_r
+    nbytes = 2 * D * d_model + 2 * T * d_model + 2 * T * D
+    flops = 2 * T * D * d_model
+    peaks, _ = load_peaks()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {
+        "ms": round(ms, 5),
+        "d_model": d_model,
+        "tokens": T,
+        "algorithmic_bytes": nbytes,
+        "gbs": round(gbs, 1),
+        "tflops": round(flops / (ms * 1e-3) / 1e12, 2),
+        "hbm_frac": round(gbs / peaks["hbm_gbs"], 4),
+        "launches": 2,
+    }
 
 
 def smi_index(local_index):

@@ -11,6 +11,10 @@
  *                      o_lat = sum_j p_j c_j, plus lse
  *   mla_out_proj       out = W_UV o_lat                  (per head)
  *
+ * mla_project_append can replace mla_append_cache when the caller holds the
+ * new tokens' hidden states: it computes c = W_DKV h and k_R = RoPE(W_KR h)
+ * and writes them straight into the cache.
+ *
  * The per-head keys W_UK c_j and values W_UV c_j of cached tokens are never
  * formed.  Sources (page title, section):
  *   - "Multi-Head Latent Attention: Low-Rank KV Compression, Decoupled RoPE,
@@ -114,6 +118,40 @@ mla_status mla_append_cache(void *cache, int num_blocks,
                             const int32_t *seqlens, const void *c_kv,
                             const void *k_r, int B, int n_new,
                             const mla_dims *dims, mla_stream_t stream);
+
+/* Bytes of device workspace mla_project_append needs (its K-split fp32
+ * partial sums: about 4 MB for 64 tokens at d_model = 5120).  Returns
+ * MLA_ERR_UNSUPPORTED for shapes mla_project_append does not take. */
+mla_status mla_project_append_workspace_size(int B, int n_new, int d_model,
+                                             const mla_dims *dims, size_t *bytes);
+
+/* Fused down-projection, RoPE and append: for token i (0 <= i < n_new) of
+ * sequence b at position p = seqlens[b] - n_new + i,
+ *   c   = W_DKV h[b,i,:]                       (d_c)
+ *   k   = W_KR h[b,i,:], then each adjacent pair (2j, 2j+1) of k rotated by
+ *         the angle p * rope_base^(-2j/d_r):  k' = k cos + rotate_half(k) sin
+ *         with rotate_half(x0, x1) = (-x1, x0)
+ * and [c ; k'] is written to the cache row of position p exactly as
+ * mla_append_cache writes it.  ("Multi-Head Latent Attention: Low-Rank KV
+ * Compression, Decoupled RoPE, and Matrix Absorption": c = W^DKV h and the
+ * shared RoPE key; "MLA, dim by dim" 3 (RoPE on adjacent pairs) and 5.2;
+ * "From Vanilla Transformers to Modern LLMs -- Part 3" 3.b, 3.k, 3.q.)
+ *   h           [B, n_new, d_model] bf16                 input
+ *   W_DKV       [d_c, d_model] bf16 (row m gives c[m])   input
+ *   W_KR        [d_r, d_model] bf16 (one k_R for all heads) input
+ *   cache, block_table, seqlens: as in mla_append_cache
+ *   workspace   >= mla_project_append_workspace_size bytes, 256-byte
+ *               aligned, caller-owned scratch (no zeroing needed)
+ * Supported: bf16, d_c = 512, d_r = 64, d_model a multiple of 64 (else
+ * MLA_ERR_UNSUPPORTED).  Products accumulate in fp32; the rotation angle is
+ * formed in double precision; the row is rounded to bf16 once.  Positions
+ * p < 0 and block entries outside [0, num_blocks) are skipped. */
+mla_status mla_project_append(const void *h, const void *W_DKV, const void *W_KR,
+                              int d_model, float rope_base, void *cache,
+                              int num_blocks, const int32_t *block_table,
+                              int max_blocks, const int32_t *seqlens, int B,
+                              int n_new, const mla_dims *dims, void *workspace,
+                              size_t workspace_bytes, mla_stream_t stream);
 
 /* Bytes of device workspace mla_decode needs for this problem size.  The
  * workspace holds the split-KV partials, the split plan and the error word.

@@ -49,6 +49,8 @@ EXPORTED = (
     "mla_get_error",
     "mla_status_string",
     "mla_decode_noalloc",
+    "mla_project_append_workspace_size",
+    "mla_project_append",
 )
 
 # size of the scratch array built into the library for mla_decode_noalloc
@@ -94,6 +96,8 @@ def _load():
         "mla_get_error": [P, P],
         "mla_status_string": [I],
         "mla_decode_noalloc": [P, P, P, I, P, I, P, I, I, I, D, P, P, P],
+        "mla_project_append_workspace_size": [I, I, I, D, ctypes.POINTER(Z)],
+        "mla_project_append": [P, P, P, I, ctypes.c_float, P, I, P, I, P, I, I, D, P, Z, P],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -150,6 +154,28 @@ def mla_append_cache(cache, num_blocks, block_table, seqlens, c_kv, k_r, dims: D
                                  block_table.shape[1], _ptr(seqlens), _ptr(c_kv), _ptr(k_r),
                                  B, n_new, ctypes.byref(dims), _stream(stream)),
            "mla_append_cache")
+
+
+def mla_project_append_workspace_size(B, n_new, d_model, dims: Dims) -> int:
+    n = ctypes.c_size_t(0)
+    _check(_lib.mla_project_append_workspace_size(B, n_new, int(d_model), ctypes.byref(dims),
+                                                  ctypes.byref(n)),
+           "mla_project_append_workspace_size")
+    return n.value
+
+
+def mla_project_append(h, W_DKV, W_KR, cache, num_blocks, block_table, seqlens, dims: Dims,
+                       workspace, rope_base=10000.0, stream=None):
+    """``[W_DKV h ; RoPE(W_KR h, p)]`` of the ``n_new`` newest tokens, written
+    into the paged cache; ``h`` is [B, n_new, d_model]."""
+    B, n_new, d_model = h.shape
+    _check(_lib.mla_project_append(_ptr(h), _ptr(W_DKV), _ptr(W_KR), int(d_model),
+                                   float(rope_base), _ptr(cache), int(num_blocks),
+                                   _ptr(block_table), block_table.shape[1], _ptr(seqlens),
+                                   B, n_new, ctypes.byref(dims), _ptr(workspace),
+                                   workspace.numel() * workspace.element_size(),
+                                   _stream(stream)),
+           "mla_project_append")
 
 
 def mla_decode_workspace_size(B, Hq, max_seqlen, dims: Dims) -> int:

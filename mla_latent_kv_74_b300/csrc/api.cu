@@ -90,6 +90,40 @@ MLA_API mla_status mla_append_cache(void *cache, int num_blocks, const int32_t *
                                    reinterpret_cast<cudaStream_t>(stream)));
 }
 
+MLA_API mla_status mla_project_append_workspace_size(int B, int n_new, int d_model,
+                                                     const mla_dims *dims, size_t *bytes) {
+  if (!bytes) return MLA_ERR_INVALID_ARG;
+  if (!dims_ok(dims)) return dims ? MLA_ERR_UNSUPPORTED : MLA_ERR_INVALID_ARG;
+  if (B < 0 || n_new < 0 || d_model < 1) return MLA_ERR_INVALID_ARG;
+  if (!tc_project_supported(*dims, d_model)) return MLA_ERR_UNSUPPORTED;
+  *bytes = project_workspace_bytes(B * n_new, d_model, *dims);
+  return MLA_OK;
+}
+
+MLA_API mla_status mla_project_append(const void *h, const void *W_DKV, const void *W_KR,
+                                      int d_model, float rope_base, void *cache, int num_blocks,
+                                      const int32_t *block_table, int max_blocks,
+                                      const int32_t *seqlens, int B, int n_new,
+                                      const mla_dims *dims, void *workspace,
+                                      size_t workspace_bytes, mla_stream_t stream) {
+  if (!dims_ok(dims)) return dims ? MLA_ERR_UNSUPPORTED : MLA_ERR_INVALID_ARG;
+  if (B < 0 || n_new < 0 || d_model < 1 || num_blocks < 1 || max_blocks < 1 ||
+      !(rope_base > 0.f))
+    return MLA_ERR_INVALID_ARG;
+  if (!tc_project_supported(*dims, d_model)) return MLA_ERR_UNSUPPORTED;
+  if (B == 0 || n_new == 0) return MLA_OK;
+  if (!h || !W_DKV || !W_KR || !cache || !block_table || !seqlens) return MLA_ERR_INVALID_ARG;
+  if (!al(h, 16) || !al(W_DKV, 16) || !al(W_KR, 16) || !al(cache, 16) || !al(block_table, 4) ||
+      !al(seqlens, 4))
+    return MLA_ERR_INVALID_ARG;
+  if (!workspace || !al(workspace, 256) ||
+      workspace_bytes < project_workspace_bytes(B * n_new, d_model, *dims))
+    return MLA_ERR_WORKSPACE;
+  return cuda_status(launch_project_append_tc(
+      h, W_DKV, W_KR, d_model, (double)rope_base, cache, num_blocks, block_table, max_blocks,
+      seqlens, B, n_new, *dims, workspace, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 MLA_API mla_status mla_decode_workspace_size(int B, int Hq, int max_seqlen, const mla_dims *dims,
                                              size_t *bytes) {
   if (!bytes) return MLA_ERR_INVALID_ARG;

@@ -10,12 +10,22 @@
 //     D[a][r] = A[a][c] B[r][c]: M = a (d_h = 128), N = r, K = d_c.
 //     Both operands K-major.
 //
+//   project  ("Multi-Head Latent Attention: Low-Rank KV Compression, Decoupled
+//   RoPE, and Matrix Absorption", the latent and RoPE-key projections;
+//   "From Vanilla Transformers to Modern LLMs -- Part 3" 3.b, 3.k):
+//     [c ; k] [t, m] = sum_x [W_DKV ; W_KR][m, x] h[t, x]
+//     D[m][t] = A[m][x] B[t][x]: M = output features, N = new tokens,
+//     K = d_model, split over the grid's y axis into fp32 partial sums that
+//     proj_finalize_kernel adds, rotates (RoPE on k) and scatters into the
+//     paged cache.
+//
 // The weights are the large operand (16.8 MB per matrix at H = 128) and are
 // read exactly once; query rows (N <= 256 per CTA) are the small one.  One
-// CTA per (128-wide M tile, head, N tile); 4 warps: warp 0 issues TMA, warp 1
-// issues MMAs, warp 2 owns the TMEM allocation, all 4 drain the accumulator
-// (warp w reads TMEM lanes 32w..32w+31).  K is streamed in 64-wide chunks
-// through a ring of shared-memory stages (full / empty mbarriers).
+// CTA per (128-wide M tile, head or K split, N tile); 4 warps: warp 0 issues
+// TMA, warp 1 issues MMAs, warp 2 owns the TMEM allocation, all 4 drain the
+// accumulator (warp w reads TMEM lanes 32w..32w+31).  K is streamed in
+// 64-wide chunks through a ring of shared-memory stages (full / empty
+// mbarriers).
 #include "internal.cuh"
 #include "ptx.cuh"
 #include "tc.cuh"
@@ -38,14 +48,22 @@ struct GemmArgs {
   int H;
   int M_total;      // output width per head: d_c (absorb) or d_h (out_proj)
   int a_rows_per_head;  // rows of the 2-D weight view per head (d_h)
+  int a_cols_per_head;  // K offset of the weight view per y index (split-K)
   int b_cols_per_head;  // columns of the 2-D activation view per head (K)
   int stages;
   __nv_bfloat16 *out;
+  // split-K mode (part != nullptr): fp32 partial sums part[y][n][m_ofs + m]
+  // of width M_total, rows m_ofs + m >= M_total dropped
+  float *part;
+  int m_ofs;
+  // M tiles from a_tiles on read their A rows from tmA2, from row 0
+  int a_tiles;
 };
 
 template <bool kAMnMajor>
 __global__ void __launch_bounds__(128, 1)
     head_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                     const __grid_constant__ CUtensorMap tmA2,
                      const __grid_constant__ CUtensorMap tmB, GemmArgs g) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte alignment of every operand tile (128B swizzle atoms).
@@ -72,6 +90,7 @@ __global__ void __launch_bounds__(128, 1)
     ptx::fence_mbar_init();
     fail = 0;
     ptx::tma_prefetch_desc(&tmA);
+    ptx::tma_prefetch_desc(&tmA2);
     ptx::tma_prefetch_desc(&tmB);
   }
   if (warp == 2) ptx::tmem_alloc(&tmem_base, ncols);
@@ -79,9 +98,15 @@ __global__ void __launch_bounds__(128, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = tmem_base;
+  // a programmatic dependent launched next may be scheduled now (it waits
+  // for this grid's completion before reading anything this grid writes)
+  ptx::launch_dependents();
 
   if (warp == 0 && ptx::elect_lane0()) {
     // ---- TMA producer ----
+    const bool second = (int)blockIdx.x >= g.a_tiles;
+    const CUtensorMap *ta = second ? &tmA2 : &tmA;
+    const int am0 = second ? ((int)blockIdx.x - g.a_tiles) * kM : m0;
     int issued = 0;
     for (int k = 0; k < g.num_k_chunks; ++k) {
       const int s = k % g.stages;
@@ -94,11 +119,12 @@ __global__ void __launch_bounds__(128, 1)
       ptx::mbar_arrive_expect_tx(&full[s], stage_bytes);
       if (kAMnMajor) {
         // two 64(M) x 64(K) boxes: M block j at +8 KB
-        ptx::tma_load_2d(a_dst, &tmA, &full[s], m0, h * g.a_rows_per_head + k * kKChunk);
-        ptx::tma_load_2d(a_dst + 8192, &tmA, &full[s], m0 + 64,
+        ptx::tma_load_2d(a_dst, ta, &full[s], am0, h * g.a_rows_per_head + k * kKChunk);
+        ptx::tma_load_2d(a_dst + 8192, ta, &full[s], am0 + 64,
                          h * g.a_rows_per_head + k * kKChunk);
       } else {
-        ptx::tma_load_2d(a_dst, &tmA, &full[s], k * kKChunk, h * g.a_rows_per_head + m0);
+        ptx::tma_load_2d(a_dst, ta, &full[s], h * g.a_cols_per_head + k * kKChunk,
+                         h * g.a_rows_per_head + am0);
       }
       ptx::tma_load_2d(b_dst, &tmB, &full[s], h * g.b_cols_per_head + k * kKChunk, n0);
       ++issued;
@@ -136,7 +162,20 @@ __global__ void __launch_bounds__(128, 1)
   const bool ok = ptx::mbar_wait(&done, 0);
   ptx::tc_fence_after();
   if (!ok) atomicExch(&fail, 1);
-  if (ok) {
+  if (ok && g.part) {
+    const int m = g.m_ofs + m0 + warp * 32 + (threadIdx.x & 31);
+    float *dst = g.part + (size_t)h * g.rows * g.M_total + m;
+    for (int c0 = 0; c0 < g.Nt; c0 += 16) {
+      float v[16];
+      ptx::tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + c0, v);
+      ptx::tmem_ld_wait();
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int n = n0 + c0 + i;
+        if (n < g.rows && m < g.M_total) dst[(size_t)n * g.M_total] = v[i];
+      }
+    }
+  } else if (ok) {
     const int m_local = warp * 32 + (threadIdx.x & 31);
     const size_t row_stride = (size_t)g.H * g.M_total;
     __nv_bfloat16 *dst = g.out + (size_t)h * g.M_total + m0 + m_local;
@@ -163,8 +202,8 @@ int pick_nt(int rows) {
 }
 
 template <bool kAMnMajor>
-cudaError_t launch_head_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, GemmArgs g,
-                             int m_tiles, cudaStream_t st) {
+cudaError_t launch_head_gemm(const CUtensorMap &tmA, const CUtensorMap &tmA2,
+                             const CUtensorMap &tmB, GemmArgs g, int m_tiles, cudaStream_t st) {
   g.stages = g.num_k_chunks < kMaxStages ? g.num_k_chunks : kMaxStages;
   const size_t smem = 1024 + (size_t)g.stages * (kABytes + g.Nt * 128);
   auto kern = head_gemm_kernel<kAMnMajor>;
@@ -172,7 +211,7 @@ cudaError_t launch_head_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, Gem
                                        (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid(m_tiles, g.H, (g.rows + g.Nt - 1) / g.Nt);
-  kern<<<grid, 128, smem, st>>>(tmA, tmB, g);
+  kern<<<grid, 128, smem, st>>>(tmA, tmA2, tmB, g);
   return cudaGetLastError();
 }
 
@@ -208,9 +247,13 @@ cudaError_t launch_absorb_tc(const void *q_nope, const void *W_UK, void *q_lat, 
   g.H = d.H;
   g.M_total = d.d_c;
   g.a_rows_per_head = d.d_h;
+  g.a_cols_per_head = 0;
   g.b_cols_per_head = d.d_h;
   g.out = static_cast<__nv_bfloat16 *>(q_lat);
-  return launch_head_gemm<true>(tmA, tmB, g, d.d_c / kM, st);
+  g.part = nullptr;
+  g.m_ofs = 0;
+  g.a_tiles = 1 << 30;
+  return launch_head_gemm<true>(tmA, tmA, tmB, g, d.d_c / kM, st);
 }
 
 cudaError_t launch_out_proj_tc(const void *o_lat, const void *W_UV, void *out, int rows,
@@ -232,9 +275,155 @@ cudaError_t launch_out_proj_tc(const void *o_lat, const void *W_UV, void *out, i
   g.H = d.H;
   g.M_total = d.d_h;
   g.a_rows_per_head = d.d_h;
+  g.a_cols_per_head = 0;
   g.b_cols_per_head = d.d_c;
   g.out = static_cast<__nv_bfloat16 *>(out);
-  return launch_head_gemm<false>(tmA, tmB, g, 1, st);
+  g.part = nullptr;
+  g.m_ofs = 0;
+  g.a_tiles = 1 << 30;
+  return launch_head_gemm<false>(tmA, tmA, tmB, g, 1, st);
+}
+
+// ---- fused latent / RoPE-key projection into the paged cache ----
+
+namespace {
+
+// Sums the K-split partials of one new token's [c ; k_R] row, rotates the
+// k_R pairs (adjacent coordinates (2p, 2p+1), angle pos * base^(-2p/d_r),
+// x cos + rotate_half(x) sin; "MLA, dim by dim" 3), and writes the row into
+// the paged cache at the token's position.  One CTA per token, one thread
+// per coordinate pair.
+__global__ void __launch_bounds__(512) proj_finalize_kernel(
+    const float *__restrict__ part, int splits, int T, int d_c, int d_r, double rope_base,
+    __nv_bfloat16 *__restrict__ cache, int num_blocks, const int32_t *__restrict__ block_table,
+    int max_blocks, const int32_t *__restrict__ seqlens, int n_new, int bs) {
+  ptx::grid_dependency_wait();  // the partial sums of the GEMM just before
+  const int t = blockIdx.x;  // token = b * n_new + i
+  const int b = t / n_new, i = t % n_new;
+  const int pos = seqlens[b] - n_new + i;
+  if (pos < 0) return;
+  const int lb = pos / bs;
+  if (lb >= max_blocks) return;
+  const int blk = block_table[(size_t)b * max_blocks + lb];
+  if (blk < 0 || blk >= num_blocks) return;  // reported by mla_decode
+  const int D = d_c + d_r;
+  const int j = threadIdx.x;  // coordinate pair 2j, 2j+1
+  if (2 * j >= D) return;
+  // eight splits' loads in flight at a time
+  const float *src = part + (size_t)t * D + 2 * j;
+  const size_t split_stride = (size_t)T * D;
+  float a0[8], a1[8];
+#pragma unroll
+  for (int u = 0; u < 8; ++u) a0[u] = a1[u] = 0.f;
+  int s = 0;
+  for (; s + 8 <= splits; s += 8) {
+    float2 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) v[u] = *reinterpret_cast<const float2 *>(src + (s + u) * split_stride);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      a0[u] += v[u].x;
+      a1[u] += v[u].y;
+    }
+  }
+  for (; s < splits; ++s) {
+    const float2 v = *reinterpret_cast<const float2 *>(src + s * split_stride);
+    a0[0] += v.x;
+    a1[0] += v.y;
+  }
+  float x0 = 0.f, x1 = 0.f;
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    x0 += a0[u];
+    x1 += a1[u];
+  }
+  if (2 * j >= d_c) {  // a RoPE pair: angle in double for long positions
+    const int p = j - d_c / 2;
+    const double ang = (double)pos * pow(rope_base, -2.0 * p / d_r);
+    double sn, cs;
+    sincos(ang, &sn, &cs);
+    const float c = (float)cs, s = (float)sn;
+    const float r0 = x0 * c - x1 * s, r1 = x1 * c + x0 * s;
+    x0 = r0;
+    x1 = r1;
+  }
+  __nv_bfloat162 o;
+  o.x = __float2bfloat16_rn(x0);
+  o.y = __float2bfloat16_rn(x1);
+  *reinterpret_cast<__nv_bfloat162 *>(cache + ((size_t)blk * bs + pos % bs) * D + 2 * j) = o;
+}
+
+constexpr int kProjMTiles = 5;  // d_c = 512 (4 tiles) + d_r = 64 (1 tile)
+
+// K chunks per split so that the M tiles x splits CTAs about fill the SMs.
+void proj_split(int d_model, int *chunks_per_split, int *splits) {
+  const int kchunks = d_model / kKChunk;
+  int cps = (kchunks * kProjMTiles + kNumSMs - 1) / kNumSMs;
+  if (cps < 1) cps = 1;
+  *chunks_per_split = cps;
+  *splits = (kchunks + cps - 1) / cps;
+}
+
+}  // namespace
+
+bool tc_project_supported(const mla_dims &d, int d_model) {
+  return d.dtype == MLA_BF16 && d.d_c == 512 && d.d_r == 64 && d_model > 0 &&
+         d_model % kKChunk == 0;
+}
+
+size_t project_workspace_bytes(int T, int d_model, const mla_dims &d) {
+  int cps, splits;
+  proj_split(d_model, &cps, &splits);
+  return (size_t)splits * T * (d.d_c + d.d_r) * sizeof(float);
+}
+
+cudaError_t launch_project_append_tc(const void *h, const void *W_DKV, const void *W_KR,
+                                     int d_model, double rope_base, void *cache, int num_blocks,
+                                     const int32_t *block_table, int max_blocks,
+                                     const int32_t *seqlens, int B, int n_new,
+                                     const mla_dims &d, void *workspace, cudaStream_t st) {
+  const int T = B * n_new;
+  int cps, splits;
+  proj_split(d_model, &cps, &splits);
+  const int Nt = pick_nt(T);
+  CUtensorMap tmDKV, tmKR, tmH;
+  // the weights as [rows][d_model], boxes of 64 x 128 rows (W_KR's 64 rows
+  // read as one tile whose upper half is out of range: zeros)
+  if (!make_tmap_2d_bf16(&tmDKV, W_DKV, d_model, d.d_c, (uint64_t)d_model * 2, 64, 128,
+                         CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap_2d_bf16(&tmKR, W_KR, d_model, d.d_r, (uint64_t)d_model * 2, 64, 128,
+                         CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap_2d_bf16(&tmH, h, d_model, T, (uint64_t)d_model * 2, 64, Nt,
+                         CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  GemmArgs g;
+  g.num_k_chunks = cps;
+  g.rows = T;
+  g.Nt = Nt;
+  g.H = splits;
+  g.M_total = d.d_c + d.d_r;
+  g.a_rows_per_head = 0;
+  g.a_cols_per_head = cps * kKChunk;
+  g.b_cols_per_head = cps * kKChunk;
+  g.out = nullptr;
+  g.part = static_cast<float *>(workspace);
+  g.m_ofs = 0;
+  g.a_tiles = d.d_c / kM;  // tiles 0-3 from W_DKV, tile 4 from W_KR
+  cudaError_t e = launch_head_gemm<false>(tmDKV, tmKR, tmH, g, kProjMTiles, st);
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(T, 1, 1);
+  cfg.blockDim = dim3((d.d_c + d.d_r) / 2, 1, 1);
+  cfg.stream = st;
+  cfg.attrs = pdl;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, proj_finalize_kernel, static_cast<const float *>(workspace),
+                            splits, T, d.d_c, d.d_r, rope_base,
+                            static_cast<__nv_bfloat16 *>(cache), num_blocks, block_table,
+                            max_blocks, seqlens, n_new, d.block_size);
 }
 
 }  // namespace mla

@@ -21,6 +21,16 @@ cudaError_t launch_decode_tc(const void *q_lat, const void *q_rope, const void *
                              const mla_dims &d, float scale, void *o_lat, float *lse,
                              void *workspace, cudaStream_t st);
 
+// bf16, d_c = 512, d_r = 64, d_model a multiple of 64 (fused latent / RoPE-key
+// projection into the paged cache on tcgen05).
+bool tc_project_supported(const mla_dims &d, int d_model);
+size_t project_workspace_bytes(int T, int d_model, const mla_dims &d);
+cudaError_t launch_project_append_tc(const void *h, const void *W_DKV, const void *W_KR,
+                                     int d_model, double rope_base, void *cache, int num_blocks,
+                                     const int32_t *block_table, int max_blocks,
+                                     const int32_t *seqlens, int B, int n_new,
+                                     const mla_dims &d, void *workspace, cudaStream_t st);
+
 // Read and clear the error word of the GEMM kernels (they take no workspace);
 // returns the device error code, or -1 if it could not be read.
 int read_and_clear_gemm_error();

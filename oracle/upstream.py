@@ -58,6 +58,19 @@ def down_project(W_DKV: np.ndarray, h: np.ndarray) -> np.ndarray:
     return project(W_DKV, h)
 
 
+def cache_row(h_t, W_DKV, W_KR, position, theta) -> np.ndarray:
+    """The cache row of one token: ``[W_DKV h_t ; RoPE(W_KR h_t, position)]``.
+
+    This is what the fused projection-and-append step writes ("Multi-Head
+    Latent Attention: ...", MLA section: the latent and the shared RoPE key;
+    "From Vanilla Transformers to Modern LLMs -- Part 3" 3.b, 3.k, 3.q: the
+    key is cached already rotated at its own position).
+    """
+    c = down_project(W_DKV, h_t)
+    k = rope(project(W_KR, h_t), position, theta)
+    return np.concatenate([c, k])
+
+
 def tiny_workload_inputs(h, W_DKV, W_KR, W_Q, W_QR, H, d_h, d_r, base=10000.0):
     """Turn the tiny workload's hidden states and weights into decode inputs.
 

@@ -230,3 +230,37 @@ def random_small(seed, H, d_h, d_c, d_r, seqlens, Hq, block_size=BLOCK_SIZE,
         "seqlens": torch.from_numpy(seqlens),
         "num_blocks": num_blocks,
     }
+
+
+def project_inputs(seed, seqlens, n_new, d_model, d_c=512, d_r=64, block_size=BLOCK_SIZE):
+    """Inputs of the fused projection-and-append step: hidden states of the
+    ``n_new`` newest tokens ``h ~ N(0,1)`` [B, n_new, d_model], weights
+    ``W_DKV`` [d_c, d_model] and ``W_KR`` [d_r, d_model] ``~ N(0, 1/d_model)``
+    (so the projected values have unit variance), and a paged cache filled
+    with N(0,1) rows that the step must overwrite only where it writes.
+    All bf16."""
+    g = _gen(seed)
+    seqlens = np.asarray(seqlens, dtype=np.int32)
+    B = len(seqlens)
+    table, num_blocks = paged_block_table(np.maximum(seqlens, 1), block_size, g)
+    out = project_tensors(g, B, n_new, d_model, d_c, d_r)
+    out.update({
+        "cache": _normal(g, (num_blocks, block_size, d_c + d_r)),
+        "block_table": torch.from_numpy(table),
+        "seqlens": torch.from_numpy(seqlens),
+        "num_blocks": num_blocks,
+    })
+    return out
+
+
+def project_tensors(g, B, n_new, d_model, d_c=512, d_r=64):
+    """``h``, ``W_DKV``, ``W_KR`` of the projection step, drawn from ``g``
+    (a seed or a ``torch.Generator``) with the recipe of ``project_inputs``."""
+    if not isinstance(g, torch.Generator):
+        g = _gen(g)
+    wstd = 1.0 / math.sqrt(d_model)
+    return {
+        "h": _normal(g, (B, n_new, d_model)),
+        "W_DKV": _normal(g, (d_c, d_model), std=wstd),
+        "W_KR": _normal(g, (d_r, d_model), std=wstd),
+    }

@@ -97,6 +97,35 @@ def test_null_and_misaligned_pointers_rejected():
     assert lib.mla_decode(*args) == m.MLA_ERR_INVALID_ARG
 
 
+def test_project_append_host_validation():
+    lib = m.raw_lib()
+    d = ctypes.byref(_dims())
+    n = ctypes.c_size_t()
+    F = ctypes.c_float
+    assert lib.mla_project_append_workspace_size(64, 1, 5120, d, ctypes.byref(n)) == m.MLA_OK
+    # 27 K splits of 3 chunks for d_model = 5120: 27 x 64 tokens x 576 fp32
+    assert n.value == 27 * 64 * 576 * 4
+    assert lib.mla_project_append_workspace_size(64, 1, 5000, d, ctypes.byref(n)) == \
+        m.MLA_ERR_UNSUPPORTED  # d_model not a multiple of 64
+    assert lib.mla_project_append_workspace_size(
+        1, 1, 512, ctypes.byref(_dims(dtype=m.MLA_FP32)), ctypes.byref(n)) == m.MLA_ERR_UNSUPPORTED
+    ok = ctypes.c_void_p(1 << 20)
+    mis = ctypes.c_void_p((1 << 20) + 2)
+    args = [ok, ok, ok, 512, F(10000.0), ok, 4, ok, 4, ok, 1, 1, d, ok, 1 << 30, None]
+    bad = list(args); bad[1] = mis
+    assert lib.mla_project_append(*bad) == m.MLA_ERR_INVALID_ARG
+    bad = list(args); bad[4] = F(0.0)
+    assert lib.mla_project_append(*bad) == m.MLA_ERR_INVALID_ARG
+    bad = list(args); bad[14] = 16
+    assert lib.mla_project_append(*bad) == m.MLA_ERR_WORKSPACE
+    bad = list(args); bad[13] = None
+    assert lib.mla_project_append(*bad) == m.MLA_ERR_WORKSPACE
+    bad = list(args); bad[3] = 100
+    assert lib.mla_project_append(*bad) == m.MLA_ERR_UNSUPPORTED
+    empty = list(args); empty[10] = 0
+    assert lib.mla_project_append(*empty) == m.MLA_OK
+
+
 def test_empty_batch_is_a_noop():
     lib = m.raw_lib()
     d = ctypes.byref(_dims())

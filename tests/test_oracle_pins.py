@@ -128,6 +128,11 @@ def check_p5_upstream():
     theta = np.array([math.pi / 2])  # the page's toy rotation: 90 degrees per position
     k_rot = np.stack([upstream.rope(k_raw[j], j, theta) for j in range(4)])
     _close(k_rot, pr["k_R_cached"]["value"], 1e-12, "cached rotated k_R (3.k)")
+    # the whole cache row of token j, as the fused projection writes it (3.q)
+    rows = np.stack([upstream.cache_row(h[j], W_DKV, W_KR, j, theta) for j in range(4)])
+    _close(rows, np.concatenate([np.array(pr["latents"]["value"], float),
+                                 np.array(pr["k_R_cached"]["value"], float)], axis=1),
+           1e-12, "cache rows [c ; k_R] (3.q)")
     W_QR = np.array(inp["W_QR"]["value"], float).T
     qr_raw = mla.project(W_QR, h[3])
     _close(qr_raw, pr["q_R_before_rotation"]["value"], EXACT, "q_R before RoPE (3.l)")
