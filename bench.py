@@ -244,6 +244,7 @@ def run_ours(args, rank, world, device):
 
     # ---- the fused projection-and-append step (measured on its own) ---------
     proj = measure_project_append(mla, args, w, dev, inp, dims, flush, stream, device)
+    oproj = measure_o_proj(mla, args, w, out, dims, flush, stream, device)
 
     # ---- reduce over ranks ----------------------------------------------------
     t_step = float(np.mean(step_ms))
@@ -330,12 +331,63 @@ def run_ours(args, rank, world, device):
     }
     if proj is not None:
         res["project_append"] = proj
+    if oproj is not None:
+        res["o_proj"] = oproj
     return res
 
 
 # hidden size of the model each workload is shaped after (DeepSeek-V2: 5120,
 # V2-Lite: 2048), for the fused projection-and-append measurement
 PROJ_D_MODEL = {"v2": 5120, "mtp": 5120, "long": 5120, "lite": 2048}
+
+
+def _time_calls(call, n, flush, stream):
+    """Mean CUDA-event time of ``n`` calls, L2 flushed before each, all
+    enqueued behind a spin kernel; three untimed calls first."""
+    for _ in range(3):
+        flush.zero_()
+        call()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n)]
+    torch.cuda.synchronize()
+    torch.cuda._sleep(int(2e6 * n))
+    for e0, e1 in evs:
+        flush.zero_()
+        e0.record(stream)
+        call()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return float(np.mean([e0.elapsed_time(e1) for e0, e1 in evs]))
+
+
+def measure_o_proj(mla, args, w, out, dims, flush, stream, device):
+    """``mla_o_proj`` on the step's head outputs (B * Hq rows of H * d_h) at the
+    model's hidden size.  Algorithmic bytes: ``W_O`` once, the head outputs
+    in and ``u`` out; FLOPs ``2 * rows * H * d_h * d_model``."""
+    d_model = PROJ_D_MODEL.get(w.name)
+    if d_model is None or w.dtype != "bf16":
+        return None
+    T, K = w.B * w.Hq, w.H * w.d_h
+    W_O = synth.o_proj_tensors(w.seed + 200, 1, 1, w.H, w.d_h, d_model)["W_O"].to(device)
+    u = torch.empty(w.B, w.Hq, d_model, dtype=torch.bfloat16, device=device)
+    ws = torch.empty(mla.mla_o_proj_workspace_size(w.B, w.Hq, d_model, dims),
+                     dtype=torch.uint8, device=device)
+    ms = _time_calls(lambda: mla.mla_o_proj(out, W_O, u, dims, ws, stream=stream),
+                     max(3, min(args.steps, 50)), flush, stream)
+    nbytes = 2 * d_model * K + 2 * T * K + 2 * T * d_model
+    flops = 2 * T * K * d_model
+    peaks, _ = load_peaks()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {
+        "ms": round(ms, 5),
+        "d_model": d_model,
+        "rows": T,
+        "algorithmic_bytes": nbytes,
+        "gbs": round(gbs, 1),
+        "tflops": round(flops / (ms * 1e-3) / 1e12, 2),
+        "hbm_frac": round(gbs / peaks["hbm_gbs"], 4),
+        "launches": 2,
+    }
 
 
 def measure_project_append(mla, args, w, dev, inp, dims, flush, stream, device):
@@ -358,21 +410,7 @@ def measure_project_append(mla, args, w, dev, inp, dims, flush, stream, device):
                                inp["num_blocks"], dev["block_table"], dev["seqlens"], dims, ws,
                                stream=stream)
 
-    for _ in range(3):
-        flush.zero_()
-        call()
-    n = max(3, min(args.steps, 50))
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(n)]
-    torch.cuda.synchronize()
-    torch.cuda._sleep(int(2e6 * n))
-    for e0, e1 in evs:
-        flush.zero_()
-        e0.record(stream)
-        call()
-        e1.record(stream)
-    torch.cuda.synchronize()
-    ms = float(np.mean([e0.elapsed_time(e1) for e0, e1 in evs]))
+    ms = _time_calls(call, max(3, min(args.steps, 50)), flush, stream)
     D = w.d_c + w.d_r
     nbytes = 2 * D * d_model + 2 * T * d_model + 2 * T * D
     flops = 2 * T * D * d_model

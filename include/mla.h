@@ -11,6 +11,7 @@
  *                      o_lat = sum_j p_j c_j, plus lse
  *   mla_out_proj       out = W_UV o_lat                  (per head)
  *
+ * mla_o_proj applies W^O to the concatenated head outputs of mla_out_proj.
  * mla_project_append can replace mla_append_cache when the caller holds the
  * new tokens' hidden states: it computes c = W_DKV h and k_R = RoPE(W_KR h)
  * and writes them straight into the cache.
@@ -152,6 +153,29 @@ mla_status mla_project_append(const void *h, const void *W_DKV, const void *W_KR
                               int max_blocks, const int32_t *seqlens, int B,
                               int n_new, const mla_dims *dims, void *workspace,
                               size_t workspace_bytes, mla_stream_t stream);
+
+/* Bytes of device workspace mla_o_proj needs (its K-split fp32 partial sums:
+ * about 9 MB for 64 rows at d_model = 5120, H = 128).  Returns
+ * MLA_ERR_UNSUPPORTED for shapes mla_o_proj does not take. */
+mla_status mla_o_proj_workspace_size(int B, int Hq, int d_model,
+                                     const mla_dims *dims, size_t *bytes);
+
+/* Output projection over the concatenated heads, the step after
+ * mla_out_proj:  u[b,i,:] = W_O [out[b,i,0,:] ; ... ; out[b,i,H-1,:]]
+ * ("Multi-Head Latent Attention: Low-Rank KV Compression, Decoupled RoPE,
+ *  and Matrix Absorption", the head outputs concatenated and multiplied by
+ *  W^O; "From Vanilla Transformers to Modern LLMs -- Part 3" 3.h, 3.p: u_t).
+ *   out         [B, Hq, H, d_h]                         input
+ *   W_O         [d_model, H * d_h] (row m gives u[m])   input
+ *   u           [B, Hq, d_model]                        output
+ *   workspace   >= mla_o_proj_workspace_size bytes, 256-byte aligned,
+ *               caller-owned scratch (no zeroing needed)
+ * Supported: bf16, d_h = 128, even d_model (else MLA_ERR_UNSUPPORTED).
+ * Products accumulate in fp32 (K split across the SMs, partials summed in
+ * fp32); u is rounded to bf16 once. */
+mla_status mla_o_proj(const void *out, const void *W_O, void *u, int B, int Hq,
+                      int d_model, const mla_dims *dims, void *workspace,
+                      size_t workspace_bytes, mla_stream_t stream);
 
 /* Bytes of device workspace mla_decode needs for this problem size.  The
  * workspace holds the split-KV partials, the split plan and the error word.

@@ -51,6 +51,8 @@ EXPORTED = (
     "mla_decode_noalloc",
     "mla_project_append_workspace_size",
     "mla_project_append",
+    "mla_o_proj_workspace_size",
+    "mla_o_proj",
 )
 
 # size of the scratch array built into the library for mla_decode_noalloc
@@ -98,6 +100,8 @@ def _load():
         "mla_decode_noalloc": [P, P, P, I, P, I, P, I, I, I, D, P, P, P],
         "mla_project_append_workspace_size": [I, I, I, D, ctypes.POINTER(Z)],
         "mla_project_append": [P, P, P, I, ctypes.c_float, P, I, P, I, P, I, I, D, P, Z, P],
+        "mla_o_proj_workspace_size": [I, I, I, D, ctypes.POINTER(Z)],
+        "mla_o_proj": [P, P, P, I, I, I, D, P, Z, P],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -176,6 +180,22 @@ def mla_project_append(h, W_DKV, W_KR, cache, num_blocks, block_table, seqlens, 
                                    workspace.numel() * workspace.element_size(),
                                    _stream(stream)),
            "mla_project_append")
+
+
+def mla_o_proj_workspace_size(B, Hq, d_model, dims: Dims) -> int:
+    n = ctypes.c_size_t(0)
+    _check(_lib.mla_o_proj_workspace_size(B, Hq, int(d_model), ctypes.byref(dims),
+                                          ctypes.byref(n)), "mla_o_proj_workspace_size")
+    return n.value
+
+
+def mla_o_proj(out, W_O, u, dims: Dims, workspace, stream=None):
+    """``u = W_O [out_0; ..; out_{H-1}]`` per row; out [B,Hq,H,d_h] -> u [B,Hq,d_model]."""
+    B, Hq = out.shape[0], out.shape[1]
+    _check(_lib.mla_o_proj(_ptr(out), _ptr(W_O), _ptr(u), B, Hq, int(W_O.shape[0]),
+                           ctypes.byref(dims), _ptr(workspace),
+                           workspace.numel() * workspace.element_size(), _stream(stream)),
+           "mla_o_proj")
 
 
 def mla_decode_workspace_size(B, Hq, max_seqlen, dims: Dims) -> int:

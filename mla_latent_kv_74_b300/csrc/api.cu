@@ -124,6 +124,32 @@ MLA_API mla_status mla_project_append(const void *h, const void *W_DKV, const vo
       seqlens, B, n_new, *dims, workspace, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+MLA_API mla_status mla_o_proj_workspace_size(int B, int Hq, int d_model, const mla_dims *dims,
+                                             size_t *bytes) {
+  if (!bytes) return MLA_ERR_INVALID_ARG;
+  if (!dims_ok(dims)) return dims ? MLA_ERR_UNSUPPORTED : MLA_ERR_INVALID_ARG;
+  if (B < 0 || Hq < 1 || d_model < 1) return MLA_ERR_INVALID_ARG;
+  if (!tc_oproj_supported(*dims, d_model)) return MLA_ERR_UNSUPPORTED;
+  *bytes = oproj_workspace_bytes(B * Hq, d_model, *dims);
+  return MLA_OK;
+}
+
+MLA_API mla_status mla_o_proj(const void *out, const void *W_O, void *u, int B, int Hq,
+                              int d_model, const mla_dims *dims, void *workspace,
+                              size_t workspace_bytes, mla_stream_t stream) {
+  if (!dims_ok(dims)) return dims ? MLA_ERR_UNSUPPORTED : MLA_ERR_INVALID_ARG;
+  if (B < 0 || Hq < 1 || d_model < 1) return MLA_ERR_INVALID_ARG;
+  if (!tc_oproj_supported(*dims, d_model)) return MLA_ERR_UNSUPPORTED;
+  if (B == 0) return MLA_OK;
+  if (!out || !W_O || !u || !al(out, 16) || !al(W_O, 16) || !al(u, 16))
+    return MLA_ERR_INVALID_ARG;
+  if (!workspace || !al(workspace, 256) ||
+      workspace_bytes < oproj_workspace_bytes(B * Hq, d_model, *dims))
+    return MLA_ERR_WORKSPACE;
+  return cuda_status(launch_oproj_tc(out, W_O, u, B * Hq, d_model, *dims, workspace,
+                                     reinterpret_cast<cudaStream_t>(stream)));
+}
+
 MLA_API mla_status mla_decode_workspace_size(int B, int Hq, int max_seqlen, const mla_dims *dims,
                                              size_t *bytes) {
   if (!bytes) return MLA_ERR_INVALID_ARG;

@@ -426,4 +426,115 @@ cudaError_t launch_project_append_tc(const void *h, const void *W_DKV, const voi
                             max_blocks, seqlens, n_new, d.block_size);
 }
 
+// ---- output projection over the concatenated heads ----
+
+namespace {
+
+// u[t, :] = bf16(sum over K splits of the fp32 partials); one thread per
+// pair of outputs, eight splits' loads in flight at a time.
+__global__ void __launch_bounds__(256) splitk_sum_kernel(const float *__restrict__ part,
+                                                         int splits, int T, int N,
+                                                         __nv_bfloat16 *__restrict__ u) {
+  ptx::grid_dependency_wait();  // the partial sums of the GEMM just before
+  const int t = blockIdx.y;
+  const int j = blockIdx.x * blockDim.x + threadIdx.x;  // output pair 2j, 2j+1
+  if (2 * j >= N) return;
+  const float *src = part + (size_t)t * N + 2 * j;
+  const size_t split_stride = (size_t)T * N;
+  float a0[8], a1[8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) a0[q] = a1[q] = 0.f;
+  int s = 0;
+  for (; s + 8 <= splits; s += 8) {
+    float2 v[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) v[q] = *reinterpret_cast<const float2 *>(src + (s + q) * split_stride);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      a0[q] += v[q].x;
+      a1[q] += v[q].y;
+    }
+  }
+  for (; s < splits; ++s) {
+    const float2 v = *reinterpret_cast<const float2 *>(src + s * split_stride);
+    a0[0] += v.x;
+    a1[0] += v.y;
+  }
+  float x0 = 0.f, x1 = 0.f;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    x0 += a0[q];
+    x1 += a1[q];
+  }
+  __nv_bfloat162 o;
+  o.x = __float2bfloat16_rn(x0);
+  o.y = __float2bfloat16_rn(x1);
+  *reinterpret_cast<__nv_bfloat162 *>(u + (size_t)t * N + 2 * j) = o;
+}
+
+// K chunks per split: about two 100 KB CTAs per SM in one wave
+void oproj_split(int K, int d_model, int *chunks_per_split, int *splits) {
+  const int kchunks = K / kKChunk;
+  const int m_tiles = (d_model + kM - 1) / kM;
+  int per_tile = (2 * kNumSMs) / m_tiles;
+  if (per_tile < 1) per_tile = 1;
+  int cps = (kchunks + per_tile - 1) / per_tile;
+  if (cps < 1) cps = 1;
+  *chunks_per_split = cps;
+  *splits = (kchunks + cps - 1) / cps;
+}
+
+}  // namespace
+
+bool tc_oproj_supported(const mla_dims &d, int d_model) {
+  return d.dtype == MLA_BF16 && d.d_h == 128 && d_model > 0 && d_model % 2 == 0;
+}
+
+size_t oproj_workspace_bytes(int T, int d_model, const mla_dims &d) {
+  int cps, splits;
+  oproj_split(d.H * d.d_h, d_model, &cps, &splits);
+  return (size_t)splits * T * d_model * sizeof(float);
+}
+
+cudaError_t launch_oproj_tc(const void *out, const void *W_O, void *u, int T, int d_model,
+                            const mla_dims &d, void *workspace, cudaStream_t st) {
+  const int K = d.H * d.d_h;
+  int cps, splits;
+  oproj_split(K, d_model, &cps, &splits);
+  const int Nt = pick_nt(T);
+  CUtensorMap tmA, tmB;
+  // W_O as [d_model rows][H*d_h], boxes of 64 x 128 rows; out as [T][H*d_h]
+  if (!make_tmap_2d_bf16(&tmA, W_O, K, d_model, (uint64_t)K * 2, 64, 128,
+                         CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap_2d_bf16(&tmB, out, K, T, (uint64_t)K * 2, 64, Nt, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  GemmArgs g;
+  g.num_k_chunks = cps;
+  g.rows = T;
+  g.Nt = Nt;
+  g.H = splits;
+  g.M_total = d_model;
+  g.a_rows_per_head = 0;
+  g.a_cols_per_head = cps * kKChunk;
+  g.b_cols_per_head = cps * kKChunk;
+  g.out = nullptr;
+  g.part = static_cast<float *>(workspace);
+  g.m_ofs = 0;
+  g.a_tiles = 1 << 30;
+  cudaError_t e = launch_head_gemm<false>(tmA, tmA, tmB, g, (d_model + kM - 1) / kM, st);
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((d_model / 2 + 255) / 256), T, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = st;
+  cfg.attrs = pdl;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, splitk_sum_kernel, static_cast<const float *>(workspace),
+                            splits, T, d_model, static_cast<__nv_bfloat16 *>(u));
+}
+
 }  // namespace mla
+

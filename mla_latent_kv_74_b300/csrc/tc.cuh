@@ -31,6 +31,13 @@ cudaError_t launch_project_append_tc(const void *h, const void *W_DKV, const voi
                                      const int32_t *seqlens, int B, int n_new,
                                      const mla_dims &d, void *workspace, cudaStream_t st);
 
+// bf16, d_h = 128, even d_model (output projection over the concatenated
+// heads on tcgen05, K split into fp32 partials).
+bool tc_oproj_supported(const mla_dims &d, int d_model);
+size_t oproj_workspace_bytes(int T, int d_model, const mla_dims &d);
+cudaError_t launch_oproj_tc(const void *out, const void *W_O, void *u, int T, int d_model,
+                            const mla_dims &d, void *workspace, cudaStream_t st);
+
 // Read and clear the error word of the GEMM kernels (they take no workspace);
 // returns the device error code, or -1 if it could not be read.
 int read_and_clear_gemm_error();

@@ -264,3 +264,14 @@ def project_tensors(g, B, n_new, d_model, d_c=512, d_r=64):
         "W_DKV": _normal(g, (d_c, d_model), std=wstd),
         "W_KR": _normal(g, (d_r, d_model), std=wstd),
     }
+
+
+def o_proj_tensors(seed, B, Hq, H, d_h, d_model):
+    """Inputs of the output projection: head outputs ``out ~ N(0,1)``
+    [B, Hq, H, d_h] and ``W_O ~ N(0, 1/(H*d_h))`` [d_model, H*d_h] (so ``u``
+    has unit variance).  bf16."""
+    g = _gen(seed)
+    return {
+        "out": _normal(g, (B, Hq, H, d_h)),
+        "W_O": _normal(g, (d_model, H * d_h), std=1.0 / math.sqrt(H * d_h)),
+    }

@@ -126,6 +126,27 @@ def test_project_append_host_validation():
     assert lib.mla_project_append(*empty) == m.MLA_OK
 
 
+def test_o_proj_host_validation():
+    lib = m.raw_lib()
+    d = ctypes.byref(_dims())
+    n = ctypes.c_size_t()
+    assert lib.mla_o_proj_workspace_size(64, 1, 5120, d, ctypes.byref(n)) == m.MLA_OK
+    # K = 128 heads x 128 = 256 chunks of 64, 40 M tiles: 7 splits of 37 chunks
+    assert n.value == 7 * 64 * 5120 * 4
+    assert lib.mla_o_proj_workspace_size(64, 1, 5121, d, ctypes.byref(n)) == m.MLA_ERR_UNSUPPORTED
+    ok = ctypes.c_void_p(1 << 20)
+    mis = ctypes.c_void_p((1 << 20) + 8)
+    args = [ok, ok, ok, 4, 1, 5120, d, ok, 1 << 30, None]
+    bad = list(args); bad[2] = mis
+    assert lib.mla_o_proj(*bad) == m.MLA_ERR_INVALID_ARG
+    bad = list(args); bad[8] = 64
+    assert lib.mla_o_proj(*bad) == m.MLA_ERR_WORKSPACE
+    bad = list(args); bad[4] = 0
+    assert lib.mla_o_proj(*bad) == m.MLA_ERR_INVALID_ARG
+    empty = list(args); empty[3] = 0
+    assert lib.mla_o_proj(*empty) == m.MLA_OK
+
+
 def test_empty_batch_is_a_noop():
     lib = m.raw_lib()
     d = ctypes.byref(_dims())
