@@ -245,6 +245,7 @@ def run_ours(args, rank, world, device):
     # ---- the fused projection-and-append step (measured on its own) ---------
     proj = measure_project_append(mla, args, w, dev, inp, dims, flush, stream, device)
     oproj = measure_o_proj(mla, args, w, out, dims, flush, stream, device)
+    qproj = measure_project_query(mla, args, w, dev, dims, flush, stream, device)
 
     # ---- reduce over ranks ----------------------------------------------------
     t_step = float(np.mean(step_ms))
@@ -333,6 +334,8 @@ def run_ours(args, rank, world, device):
         res["project_append"] = proj
     if oproj is not None:
         res["o_proj"] = oproj
+    if qproj is not None:
+        res["project_query"] = qproj
     return res
 
 
@@ -358,6 +361,39 @@ def _time_calls(call, n, flush, stream):
         e1.record(stream)
     torch.cuda.synchronize()
     return float(np.mean([e0.elapsed_time(e1) for e0, e1 in evs]))
+
+
+def measure_project_query(mla, args, w, dev, dims, flush, stream, device):
+    """``mla_project_query`` for the step's B * Hq query rows at the model's
+    hidden size.  Algorithmic bytes: ``W_Q`` and ``W_QR`` once, ``h`` in,
+    ``q_nope`` and ``q_rope`` out; FLOPs ``2 * rows * H * (d_h + d_r) * d_model``."""
+    d_model = PROJ_D_MODEL.get(w.name)
+    if d_model is None or w.dtype != "bf16":
+        return None
+    T, M = w.B * w.Hq, w.H * (w.d_h + w.d_r)
+    t = {k: v.to(device) for k, v in synth.query_tensors(w.seed + 300, w.B, w.Hq, w.H, w.d_h,
+                                                          w.d_r, d_model).items()}
+    q_nope = torch.empty(w.B, w.Hq, w.H, w.d_h, dtype=torch.bfloat16, device=device)
+    q_rope = torch.empty(w.B, w.Hq, w.H, w.d_r, dtype=torch.bfloat16, device=device)
+    ws = torch.empty(mla.mla_project_query_workspace_size(w.B, w.Hq, d_model, dims),
+                     dtype=torch.uint8, device=device)
+    ms = _time_calls(lambda: mla.mla_project_query(t["h"], t["W_Q"], t["W_QR"], dev["seqlens"],
+                                                   dims, q_nope, q_rope, ws, stream=stream),
+                     max(3, min(args.steps, 50)), flush, stream)
+    nbytes = 2 * M * d_model + 2 * T * d_model + 2 * T * M
+    flops = 2 * T * M * d_model
+    peaks, _ = load_peaks()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {
+        "ms": round(ms, 5),
+        "d_model": d_model,
+        "rows": T,
+        "algorithmic_bytes": nbytes,
+        "gbs": round(gbs, 1),
+        "tflops": round(flops / (ms * 1e-3) / 1e12, 2),
+        "hbm_frac": round(gbs / peaks["hbm_gbs"], 4),
+        "launches": 2,
+    }
 
 
 def measure_o_proj(mla, args, w, out, dims, flush, stream, device):

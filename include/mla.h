@@ -11,6 +11,7 @@
  *                      o_lat = sum_j p_j c_j, plus lse
  *   mla_out_proj       out = W_UV o_lat                  (per head)
  *
+ * mla_project_query produces q_nope and q_rope from the hidden states.
  * mla_o_proj applies W^O to the concatenated head outputs of mla_out_proj.
  * mla_project_append can replace mla_append_cache when the caller holds the
  * new tokens' hidden states: it computes c = W_DKV h and k_R = RoPE(W_KR h)
@@ -153,6 +154,38 @@ mla_status mla_project_append(const void *h, const void *W_DKV, const void *W_KR
                               int max_blocks, const int32_t *seqlens, int B,
                               int n_new, const mla_dims *dims, void *workspace,
                               size_t workspace_bytes, mla_stream_t stream);
+
+/* Bytes of device workspace mla_project_query needs (its K-split fp32
+ * partial sums: about 19 MB for 64 rows at H = 128, d_model = 5120).  Returns
+ * MLA_ERR_UNSUPPORTED for shapes mla_project_query does not take. */
+mla_status mla_project_query_workspace_size(int B, int Hq, int d_model,
+                                            const mla_dims *dims, size_t *bytes);
+
+/* The query side of the step, before mla_absorb_query (no query
+ * compression, as in DeepSeek-V2-Lite): for query slot i of sequence b at
+ * position p = seqlens[b] - Hq + i,
+ *   q_nope[b,i,:,:] = W_Q h[b,i,:]                     (H * d_h)
+ *   q_rope[b,i,h,:] = RoPE((W_QR h[b,i,:])[h*d_r .. h*d_r+d_r-1], p)
+ * with RoPE as in mla_project_append (pairs (2j, 2j+1) of each head's d_r,
+ * angle p * rope_base^(-2j/d_r)).  ("Multi-Head Latent Attention: Low-Rank
+ * KV Compression, Decoupled RoPE, and Matrix Absorption": the query and its
+ * per-head RoPE part; "From Vanilla Transformers to Modern LLMs -- Part 3"
+ * 3.d, 3.l; "MLA, dim by dim" 3, 5.2.)
+ *   h       [B, Hq, d_model] bf16                      input
+ *   W_Q     [H * d_h, d_model] bf16 (row m gives q[m])  input
+ *   W_QR    [H * d_r, d_model] bf16                    input
+ *   q_nope  [B, Hq, H, d_h], q_rope [B, Hq, H, d_r]   output (the inputs of
+ *           mla_absorb_query and mla_decode)
+ *   workspace >= mla_project_query_workspace_size bytes, 256-byte aligned
+ * Supported: bf16, d_h = 128, even d_r, d_model a multiple of 64.  Products
+ * accumulate in fp32, the angle is formed in double precision, outputs are
+ * rounded to bf16 once. */
+mla_status mla_project_query(const void *h, const void *W_Q, const void *W_QR,
+                             int d_model, float rope_base,
+                             const int32_t *seqlens, int B, int Hq,
+                             const mla_dims *dims, void *q_nope, void *q_rope,
+                             void *workspace, size_t workspace_bytes,
+                             mla_stream_t stream);
 
 /* Bytes of device workspace mla_o_proj needs (its K-split fp32 partial sums:
  * about 9 MB for 64 rows at d_model = 5120, H = 128).  Returns

@@ -53,6 +53,8 @@ EXPORTED = (
     "mla_project_append",
     "mla_o_proj_workspace_size",
     "mla_o_proj",
+    "mla_project_query_workspace_size",
+    "mla_project_query",
 )
 
 # size of the scratch array built into the library for mla_decode_noalloc
@@ -102,6 +104,8 @@ def _load():
         "mla_project_append": [P, P, P, I, ctypes.c_float, P, I, P, I, P, I, I, D, P, Z, P],
         "mla_o_proj_workspace_size": [I, I, I, D, ctypes.POINTER(Z)],
         "mla_o_proj": [P, P, P, I, I, I, D, P, Z, P],
+        "mla_project_query_workspace_size": [I, I, I, D, ctypes.POINTER(Z)],
+        "mla_project_query": [P, P, P, I, ctypes.c_float, P, I, I, D, P, P, P, Z, P],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -180,6 +184,26 @@ def mla_project_append(h, W_DKV, W_KR, cache, num_blocks, block_table, seqlens, 
                                    workspace.numel() * workspace.element_size(),
                                    _stream(stream)),
            "mla_project_append")
+
+
+def mla_project_query_workspace_size(B, Hq, d_model, dims: Dims) -> int:
+    n = ctypes.c_size_t(0)
+    _check(_lib.mla_project_query_workspace_size(B, Hq, int(d_model), ctypes.byref(dims),
+                                                 ctypes.byref(n)),
+           "mla_project_query_workspace_size")
+    return n.value
+
+
+def mla_project_query(h, W_Q, W_QR, seqlens, dims: Dims, q_nope, q_rope, workspace,
+                      rope_base=10000.0, stream=None):
+    """``q_nope = W_Q h``, ``q_rope = RoPE(W_QR h, p)`` per head; ``h`` [B,Hq,d_model]."""
+    B, Hq, d_model = h.shape
+    _check(_lib.mla_project_query(_ptr(h), _ptr(W_Q), _ptr(W_QR), int(d_model),
+                                  float(rope_base), _ptr(seqlens), B, Hq, ctypes.byref(dims),
+                                  _ptr(q_nope), _ptr(q_rope), _ptr(workspace),
+                                  workspace.numel() * workspace.element_size(),
+                                  _stream(stream)),
+           "mla_project_query")
 
 
 def mla_o_proj_workspace_size(B, Hq, d_model, dims: Dims) -> int:

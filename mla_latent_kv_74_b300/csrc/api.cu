@@ -150,6 +150,37 @@ MLA_API mla_status mla_o_proj(const void *out, const void *W_O, void *u, int B, 
                                      reinterpret_cast<cudaStream_t>(stream)));
 }
 
+MLA_API mla_status mla_project_query_workspace_size(int B, int Hq, int d_model,
+                                                    const mla_dims *dims, size_t *bytes) {
+  if (!bytes) return MLA_ERR_INVALID_ARG;
+  if (!dims_ok(dims)) return dims ? MLA_ERR_UNSUPPORTED : MLA_ERR_INVALID_ARG;
+  if (B < 0 || Hq < 1 || d_model < 1) return MLA_ERR_INVALID_ARG;
+  if (!tc_qproj_supported(*dims, d_model)) return MLA_ERR_UNSUPPORTED;
+  *bytes = qproj_workspace_bytes(B * Hq, d_model, *dims);
+  return MLA_OK;
+}
+
+MLA_API mla_status mla_project_query(const void *h, const void *W_Q, const void *W_QR,
+                                     int d_model, float rope_base, const int32_t *seqlens, int B,
+                                     int Hq, const mla_dims *dims, void *q_nope, void *q_rope,
+                                     void *workspace, size_t workspace_bytes,
+                                     mla_stream_t stream) {
+  if (!dims_ok(dims)) return dims ? MLA_ERR_UNSUPPORTED : MLA_ERR_INVALID_ARG;
+  if (B < 0 || Hq < 1 || d_model < 1 || !(rope_base > 0.f)) return MLA_ERR_INVALID_ARG;
+  if (!tc_qproj_supported(*dims, d_model)) return MLA_ERR_UNSUPPORTED;
+  if (B == 0) return MLA_OK;
+  if (!h || !W_Q || !W_QR || !seqlens || !q_nope || !q_rope) return MLA_ERR_INVALID_ARG;
+  if (!al(h, 16) || !al(W_Q, 16) || !al(W_QR, 16) || !al(seqlens, 4) || !al(q_nope, 16) ||
+      !al(q_rope, 16))
+    return MLA_ERR_INVALID_ARG;
+  if (!workspace || !al(workspace, 256) ||
+      workspace_bytes < qproj_workspace_bytes(B * Hq, d_model, *dims))
+    return MLA_ERR_WORKSPACE;
+  return cuda_status(launch_qproj_tc(h, W_Q, W_QR, d_model, (double)rope_base, seqlens, B, Hq,
+                                     *dims, q_nope, q_rope, workspace,
+                                     reinterpret_cast<cudaStream_t>(stream)));
+}
+
 MLA_API mla_status mla_decode_workspace_size(int B, int Hq, int max_seqlen, const mla_dims *dims,
                                              size_t *bytes) {
   if (!bytes) return MLA_ERR_INVALID_ARG;

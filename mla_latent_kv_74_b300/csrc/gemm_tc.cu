@@ -288,13 +288,37 @@ cudaError_t launch_out_proj_tc(const void *o_lat, const void *W_UV, void *out, i
 
 namespace {
 
+// RoPE frequencies theta_j = base^(-2j/d_r), j < d_r/2, formed on the host in
+// double precision and passed by value.
+struct RopeTable {
+  double theta[64];
+};
+
+RopeTable rope_table(double base, int d_r) {
+  RopeTable t = {};
+  for (int j = 0; j < d_r / 2 && j < 64; ++j) t.theta[j] = pow(base, -2.0 * j / d_r);
+  return t;
+}
+
+// cos and sin of pos * theta: the angle is formed in double precision and
+// brought into [-pi, pi] by subtracting the nearest multiple of 2 pi (2 pi
+// split into a double head and tail), then evaluated in fp32.
+__device__ __forceinline__ void rope_cos_sin(int pos, double theta, float *c, float *s) {
+  constexpr double kTwoPiHi = 6.283185307179586;       // 2 pi rounded to double
+  constexpr double kTwoPiLo = 2.4492935982947064e-16;  // 2 pi minus kTwoPiHi
+  const double ang = (double)pos * theta;
+  const double k = rint(ang * (1.0 / kTwoPiHi));
+  const double r = fma(-k, kTwoPiLo, fma(-k, kTwoPiHi, ang));
+  sincosf((float)r, s, c);
+}
+
 // Sums the K-split partials of one new token's [c ; k_R] row, rotates the
 // k_R pairs (adjacent coordinates (2p, 2p+1), angle pos * base^(-2p/d_r),
 // x cos + rotate_half(x) sin; "MLA, dim by dim" 3), and writes the row into
 // the paged cache at the token's position.  One CTA per token, one thread
 // per coordinate pair.
 __global__ void __launch_bounds__(512) proj_finalize_kernel(
-    const float *__restrict__ part, int splits, int T, int d_c, int d_r, double rope_base,
+    const float *__restrict__ part, int splits, int T, int d_c, int d_r, RopeTable rope,
     __nv_bfloat16 *__restrict__ cache, int num_blocks, const int32_t *__restrict__ block_table,
     int max_blocks, const int32_t *__restrict__ seqlens, int n_new, int bs) {
   ptx::grid_dependency_wait();  // the partial sums of the GEMM just before
@@ -337,12 +361,9 @@ __global__ void __launch_bounds__(512) proj_finalize_kernel(
     x0 += a0[u];
     x1 += a1[u];
   }
-  if (2 * j >= d_c) {  // a RoPE pair: angle in double for long positions
-    const int p = j - d_c / 2;
-    const double ang = (double)pos * pow(rope_base, -2.0 * p / d_r);
-    double sn, cs;
-    sincos(ang, &sn, &cs);
-    const float c = (float)cs, s = (float)sn;
+  if (2 * j >= d_c) {  // a RoPE pair
+    float c, s;
+    rope_cos_sin(pos, rope.theta[j - d_c / 2], &c, &s);
     const float r0 = x0 * c - x1 * s, r1 = x1 * c + x0 * s;
     x0 = r0;
     x1 = r1;
@@ -421,7 +442,7 @@ cudaError_t launch_project_append_tc(const void *h, const void *W_DKV, const voi
   cfg.attrs = pdl;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, proj_finalize_kernel, static_cast<const float *>(workspace),
-                            splits, T, d.d_c, d.d_r, rope_base,
+                            splits, T, d.d_c, d.d_r, rope_table(rope_base, d.d_r),
                             static_cast<__nv_bfloat16 *>(cache), num_blocks, block_table,
                             max_blocks, seqlens, n_new, d.block_size);
 }
@@ -472,16 +493,33 @@ __global__ void __launch_bounds__(256) splitk_sum_kernel(const float *__restrict
   *reinterpret_cast<__nv_bfloat162 *>(u + (size_t)t * N + 2 * j) = o;
 }
 
-// K chunks per split: about two 100 KB CTAs per SM in one wave
-void oproj_split(int K, int d_model, int *chunks_per_split, int *splits) {
-  const int kchunks = K / kKChunk;
-  const int m_tiles = (d_model + kM - 1) / kM;
-  int per_tile = (2 * kNumSMs) / m_tiles;
-  if (per_tile < 1) per_tile = 1;
-  int cps = (kchunks + per_tile - 1) / per_tile;
-  if (cps < 1) cps = 1;
-  *chunks_per_split = cps;
-  *splits = (kchunks + cps - 1) / cps;
+// K split of a weight-streaming GEMM with T rows and M outputs.  Each CTA
+// streams its chunks at a latency-bound rate (measured: about 1.1 us per
+// 16 KB chunk with two ~100 KB CTAs per SM), and every split adds T x M fp32
+// partials written and read back (taken at 6 TB/s).  Estimated time:
+// (waves of 2 x 148 CTAs) x (chunks per CTA) x 1.1 us + splits x T x M x 8 B
+// / 6 TB/s; take the split that minimises it.
+void choose_split(int kchunks, int m_tiles, int T, int M, int *chunks_per_split, int *splits) {
+  const int slots = 2 * kNumSMs;
+  const double partial_us = (double)T * M * 8.0 / 6e6;
+  int best_s = 1;
+  double best = -1.0;
+  for (int s = 1; s <= kchunks; ++s) {
+    const int cps = (kchunks + s - 1) / s;
+    if ((kchunks + cps - 1) / cps != s) continue;  // same as a smaller split
+    const long waves = ((long)m_tiles * s + slots - 1) / slots;
+    const double cost = (double)waves * cps * 1.1 + s * partial_us;
+    if (best < 0.0 || cost < best) {
+      best = cost;
+      best_s = s;
+    }
+  }
+  *chunks_per_split = (kchunks + best_s - 1) / best_s;
+  *splits = best_s;
+}
+
+void oproj_split(int K, int d_model, int T, int *chunks_per_split, int *splits) {
+  choose_split(K / kKChunk, (d_model + kM - 1) / kM, T, d_model, chunks_per_split, splits);
 }
 
 }  // namespace
@@ -492,7 +530,7 @@ bool tc_oproj_supported(const mla_dims &d, int d_model) {
 
 size_t oproj_workspace_bytes(int T, int d_model, const mla_dims &d) {
   int cps, splits;
-  oproj_split(d.H * d.d_h, d_model, &cps, &splits);
+  oproj_split(d.H * d.d_h, d_model, T, &cps, &splits);
   return (size_t)splits * T * d_model * sizeof(float);
 }
 
@@ -500,7 +538,7 @@ cudaError_t launch_oproj_tc(const void *out, const void *W_O, void *u, int T, in
                             const mla_dims &d, void *workspace, cudaStream_t st) {
   const int K = d.H * d.d_h;
   int cps, splits;
-  oproj_split(K, d_model, &cps, &splits);
+  oproj_split(K, d_model, T, &cps, &splits);
   const int Nt = pick_nt(T);
   CUtensorMap tmA, tmB;
   // W_O as [d_model rows][H*d_h], boxes of 64 x 128 rows; out as [T][H*d_h]
@@ -536,5 +574,117 @@ cudaError_t launch_oproj_tc(const void *out, const void *W_O, void *u, int T, in
                             splits, T, d_model, static_cast<__nv_bfloat16 *>(u));
 }
 
+// ---- query projections ----
+
+namespace {
+
+// q_nope = bf16(sum of partials) for features < H*d_h; q_rope = the RoPE'd
+// rest, head by head (pairs (2j, 2j+1) of each head's d_r, angle
+// pos * base^(-2j/d_r)).  Query slot i of sequence b sits at position
+// seqlens[b] - Hq + i.  One thread per feature pair.
+__global__ void __launch_bounds__(256) qproj_finalize_kernel(
+    const float *__restrict__ part, int splits, int T, int Hd, int Hr, int d_r,
+    RopeTable rope, const int32_t *__restrict__ seqlens, int Hq,
+    __nv_bfloat16 *__restrict__ q_nope, __nv_bfloat16 *__restrict__ q_rope) {
+  ptx::grid_dependency_wait();  // the partial sums of the GEMM just before
+  const int t = blockIdx.y;
+  const int M = Hd + Hr;
+  const int j = blockIdx.x * blockDim.x + threadIdx.x;  // feature pair 2j, 2j+1
+  if (2 * j >= M) return;
+  const float *src = part + (size_t)t * M + 2 * j;
+  const size_t split_stride = (size_t)T * M;
+  float x0 = 0.f, x1 = 0.f;
+  for (int s = 0; s < splits; ++s) {
+    const float2 v = *reinterpret_cast<const float2 *>(src + s * split_stride);
+    x0 += v.x;
+    x1 += v.y;
+  }
+  __nv_bfloat162 o;
+  if (2 * j < Hd) {
+    o.x = __float2bfloat16_rn(x0);
+    o.y = __float2bfloat16_rn(x1);
+    *reinterpret_cast<__nv_bfloat162 *>(q_nope + (size_t)t * Hd + 2 * j) = o;
+    return;
+  }
+  const int f = 2 * j - Hd;               // feature within the RoPE part
+  const int p = (f % d_r) / 2;            // pair within the head
+  const int b = t / Hq, i = t % Hq;
+  const int pos = seqlens[b] - Hq + i;
+  float c, sv;
+  rope_cos_sin(pos, rope.theta[p], &c, &sv);
+  o.x = __float2bfloat16_rn(x0 * c - x1 * sv);
+  o.y = __float2bfloat16_rn(x1 * c + x0 * sv);
+  *reinterpret_cast<__nv_bfloat162 *>(q_rope + (size_t)t * Hr + f) = o;
+}
+
+void qproj_split(int d_model, int m_tiles, int T, int M, int *chunks_per_split, int *splits) {
+  choose_split(d_model / kKChunk, m_tiles, T, M, chunks_per_split, splits);
+}
+
+int qproj_m_tiles(const mla_dims &d) {
+  return (d.H * d.d_h) / kM + (d.H * d.d_r + kM - 1) / kM;
+}
+
+}  // namespace
+
+bool tc_qproj_supported(const mla_dims &d, int d_model) {
+  return d.dtype == MLA_BF16 && d.d_h == 128 && d.d_r > 0 && d.d_r <= 128 && d.d_r % 2 == 0 &&
+         d_model > 0 &&
+         d_model % kKChunk == 0;
+}
+
+size_t qproj_workspace_bytes(int T, int d_model, const mla_dims &d) {
+  int cps, splits;
+  qproj_split(d_model, qproj_m_tiles(d), T, d.H * (d.d_h + d.d_r), &cps, &splits);
+  return (size_t)splits * T * d.H * (d.d_h + d.d_r) * sizeof(float);
+}
+
+cudaError_t launch_qproj_tc(const void *h, const void *W_Q, const void *W_QR, int d_model,
+                            double rope_base, const int32_t *seqlens, int B, int Hq,
+                            const mla_dims &d, void *q_nope, void *q_rope, void *workspace,
+                            cudaStream_t st) {
+  const int T = B * Hq, Hd = d.H * d.d_h, Hr = d.H * d.d_r;
+  int cps, splits;
+  qproj_split(d_model, qproj_m_tiles(d), T, Hd + Hr, &cps, &splits);
+  const int Nt = pick_nt(T);
+  CUtensorMap tmQ, tmQR, tmH;
+  if (!make_tmap_2d_bf16(&tmQ, W_Q, d_model, Hd, (uint64_t)d_model * 2, 64, 128,
+                         CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap_2d_bf16(&tmQR, W_QR, d_model, Hr, (uint64_t)d_model * 2, 64, 128,
+                         CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap_2d_bf16(&tmH, h, d_model, T, (uint64_t)d_model * 2, 64, Nt,
+                         CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  GemmArgs g;
+  g.num_k_chunks = cps;
+  g.rows = T;
+  g.Nt = Nt;
+  g.H = splits;
+  g.M_total = Hd + Hr;
+  g.a_rows_per_head = 0;
+  g.a_cols_per_head = cps * kKChunk;
+  g.b_cols_per_head = cps * kKChunk;
+  g.out = nullptr;
+  g.part = static_cast<float *>(workspace);
+  g.m_ofs = 0;
+  g.a_tiles = Hd / kM;  // W_Q rows, then W_QR rows
+  cudaError_t e = launch_head_gemm<false>(tmQ, tmQR, tmH, g, qproj_m_tiles(d), st);
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(((Hd + Hr) / 2 + 255) / 256), T, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = st;
+  cfg.attrs = pdl;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, qproj_finalize_kernel, static_cast<const float *>(workspace),
+                            splits, T, Hd, Hr, d.d_r, rope_table(rope_base, d.d_r), seqlens, Hq,
+                            static_cast<__nv_bfloat16 *>(q_nope),
+                            static_cast<__nv_bfloat16 *>(q_rope));
+}
+
 }  // namespace mla
+
 

@@ -38,6 +38,15 @@ size_t oproj_workspace_bytes(int T, int d_model, const mla_dims &d);
 cudaError_t launch_oproj_tc(const void *out, const void *W_O, void *u, int T, int d_model,
                             const mla_dims &d, void *workspace, cudaStream_t st);
 
+// bf16, d_h = 128, even d_r, d_model a multiple of 64 (query projections
+// q_nope = W_Q h and q_rope = RoPE(W_QR h) on tcgen05).
+bool tc_qproj_supported(const mla_dims &d, int d_model);
+size_t qproj_workspace_bytes(int T, int d_model, const mla_dims &d);
+cudaError_t launch_qproj_tc(const void *h, const void *W_Q, const void *W_QR, int d_model,
+                            double rope_base, const int32_t *seqlens, int B, int Hq,
+                            const mla_dims &d, void *q_nope, void *q_rope, void *workspace,
+                            cudaStream_t st);
+
 // Read and clear the error word of the GEMM kernels (they take no workspace);
 // returns the device error code, or -1 if it could not be read.
 int read_and_clear_gemm_error();

@@ -71,6 +71,18 @@ def cache_row(h_t, W_DKV, W_KR, position, theta) -> np.ndarray:
     return np.concatenate([c, k])
 
 
+def query_projection(h_t, W_Q, W_QR, H, d_h, d_r, position, theta):
+    """The query of one token: ``q_nope[h] = (W_Q h_t)[h*d_h:(h+1)*d_h]`` and
+    ``q_rope[h] = RoPE((W_QR h_t)[h*d_r:(h+1)*d_r], position)`` (no query
+    compression; "Multi-Head Latent Attention: ...", the query and its
+    per-head RoPE part; "From Vanilla Transformers to Modern LLMs -- Part 3"
+    3.d, 3.l).  Returns ``(q_nope [H, d_h], q_rope [H, d_r])``."""
+    q = project(W_Q, h_t).reshape(H, d_h)
+    qr = project(W_QR, h_t)
+    q_rope = np.stack([rope(qr[i * d_r:(i + 1) * d_r], position, theta) for i in range(H)])
+    return q, q_rope
+
+
 def tiny_workload_inputs(h, W_DKV, W_KR, W_Q, W_QR, H, d_h, d_r, base=10000.0):
     """Turn the tiny workload's hidden states and weights into decode inputs.
 

@@ -275,3 +275,16 @@ def o_proj_tensors(seed, B, Hq, H, d_h, d_model):
         "out": _normal(g, (B, Hq, H, d_h)),
         "W_O": _normal(g, (d_model, H * d_h), std=1.0 / math.sqrt(H * d_h)),
     }
+
+
+def query_tensors(seed, B, Hq, H, d_h, d_r, d_model):
+    """Inputs of the query projections: ``h ~ N(0,1)`` [B, Hq, d_model] and
+    ``W_Q`` [H*d_h, d_model], ``W_QR`` [H*d_r, d_model] ``~ N(0, 1/d_model)``.
+    bf16."""
+    g = _gen(seed)
+    wstd = 1.0 / math.sqrt(d_model)
+    return {
+        "h": _normal(g, (B, Hq, d_model)),
+        "W_Q": _normal(g, (H * d_h, d_model), std=wstd),
+        "W_QR": _normal(g, (H * d_r, d_model), std=wstd),
+    }

@@ -147,6 +147,30 @@ def test_o_proj_host_validation():
     assert lib.mla_o_proj(*empty) == m.MLA_OK
 
 
+def test_project_query_host_validation():
+    lib = m.raw_lib()
+    d = ctypes.byref(_dims())
+    n = ctypes.c_size_t()
+    F = ctypes.c_float
+    assert lib.mla_project_query_workspace_size(64, 1, 5120, d, ctypes.byref(n)) == m.MLA_OK
+    # 128 + 64 M tiles, 80 K chunks: three splits of 27 chunks (two waves of
+    # 296 CTAs beat one slow wave), 64 rows x 128 heads x (128 + 64) fp32 each
+    assert n.value == 3 * 64 * 128 * 192 * 4
+    assert lib.mla_project_query_workspace_size(64, 1, 5000, d, ctypes.byref(n)) == \
+        m.MLA_ERR_UNSUPPORTED
+    ok = ctypes.c_void_p(1 << 20)
+    mis = ctypes.c_void_p((1 << 20) + 4)
+    args = [ok, ok, ok, 512, F(10000.0), ok, 2, 1, d, ok, ok, ok, 1 << 30, None]
+    bad = list(args); bad[10] = mis
+    assert lib.mla_project_query(*bad) == m.MLA_ERR_INVALID_ARG
+    bad = list(args); bad[12] = 16
+    assert lib.mla_project_query(*bad) == m.MLA_ERR_WORKSPACE
+    bad = list(args); bad[4] = F(-1.0)
+    assert lib.mla_project_query(*bad) == m.MLA_ERR_INVALID_ARG
+    empty = list(args); empty[6] = 0
+    assert lib.mla_project_query(*empty) == m.MLA_OK
+
+
 def test_empty_batch_is_a_noop():
     lib = m.raw_lib()
     d = ctypes.byref(_dims())

@@ -143,6 +143,11 @@ def check_p5_upstream():
     both = mla.dot(upstream.rope(qr_raw[0:2], 3, theta), upstream.rope(k_raw[2], 2, theta))
     rel = mla.dot(upstream.rope(qr_raw[0:2], 1, theta), k_raw[2])
     _close([both, rel], [pr["relative_position_score"]["value"]] * 2, 1e-12, "relative position (3.n)")
+    # the query of token 4 (position 3) as the query projection builds it
+    # (3.d, 3.l): content query and the per-head rotated RoPE queries
+    qn, qr = upstream.query_projection(h[3], Wq, W_QR, 2, 2, 2, 3, theta)
+    _close(qn.reshape(-1), pr["q4"]["value"], EXACT, "q4 by heads (3.d)")
+    _close(qr, [pr["q_R_head1"]["value"], pr["q_R_head2"]["value"]], 1e-12, "q_R heads (3.l)")
 
 
 def check_p5_content_path():
