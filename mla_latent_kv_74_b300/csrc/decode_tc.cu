@@ -12,17 +12,21 @@
 // latent accumulator O (128 heads x 512) or the full query, not both:
 //   * the S-CTA (cluster rank 1) keeps the item's query [q_lat ; q_rope]
 //     (128 x 576 bf16 = 288 columns) in TMEM as the A operand of
-//     S = Q C^T (M=128, N=64, K=576; three S buffers in the other columns),
-//     runs the online softmax and ships P (bf16) to its peer;
+//     S = Q C^T (M=128, N=64, K=576; three 64-column partial-score buffers
+//     in the other columns), runs the online softmax and ships P (bf16) to
+//     its peer;
 //   * the V-CTA (rank 0) keeps O (512 columns) in TMEM and accumulates
 //     O += P C (M=128, N=2x256, K=64) with P in its shared memory.
-// Each CTA streams the cache through its own ring of shared-memory stages:
-// the S-CTA loads [c_KV ; k_R] tiles (HBM) and frees a stage as soon as its
-// QK^T is done; the V-CTA loads the latent part of the same tiles a little
-// later (L2 hits) and frees a stage after its PV.  Decoupling the rings keeps
-// the long HBM latency off the softmax -> PV chain.  Two warps of the S-CTA
-// issue QK^T for alternate tiles, so two accumulation chains keep the tensor
-// pipe busy at N = 64.
+// Each CTA streams the cache through its own ring of shared-memory stages,
+// one 3-D TMA copy per stage: the S-CTA loads [c_KV ; k_R] tiles (HBM) and
+// frees a stage as soon as its QK^T is done; the V-CTA loads the latent part
+// of the same tiles a little later (L2 hits) and frees a stage after its PV.
+// Decoupling the rings keeps the long HBM latency off the softmax -> PV
+// chain.  Each segment's query reaches the S-CTA through its ring too (two
+// stages ahead of the segment's tiles), copied into TMEM by a softmax group.
+// Two warps of the S-CTA each issue half of every tile's k-steps into their
+// own partial-score buffer (one thread cannot issue N = 64 MMAs at the
+// tensor pipe's rate, two can); the softmax adds the two partials.
 //
 // P goes straight into the V-CTA's shared memory by st.async (distributed
 // shared memory, counted on the destination mbarrier), already in the
@@ -35,7 +39,7 @@
 // their own row sums, and merge them at each segment end before the row
 // statistics go to the V-CTA (st.async).  The V-CTA's correction warps apply
 // the rare O rescales and run each segment's epilogue, staging O through the
-// last tile's P buffer and writing it with TMA stores.
+// last tile's P buffer and writing whole 128-byte row pieces.
 //
 // Online softmax in base 2 with lazy rescaling: the running maximum moves
 // (and O is rescaled by the V-CTA's correction warps) only when a tile's
@@ -52,6 +56,8 @@
 // and MMA issuer; S-CTA: warp 6 second QK^T issuer, warps 2-5 and 7-10 the
 // two softmax groups (even / odd tiles); V-CTA: warps 2-5 rescale and
 // epilogue.  A warp w that touches TMEM owns lanes 32*(w%4) .. 32*(w%4)+31.
+// The kernel is launched as a programmatic dependent of the previous kernel
+// in the stream and waits for it only after its barrier and TMEM setup.
 //
 // Every wait is bounded; a lost wait records MLA_ERR_TIMEOUT in the
 // workspace, tells the peer CTA to stop, and the CTA unwinds (no trap).
