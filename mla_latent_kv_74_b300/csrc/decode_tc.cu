@@ -80,6 +80,12 @@ constexpr int kMaxItems = 1024;    // B * Hq limit of this path
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2(256)
+// The split plan charges each item's start (its query load and, for the pair
+// that also ends an item there, an epilogue: about 9 us against 1.2 us per
+// tile, measured) as this many extra tiles, so pairs that cross an item
+// boundary get fewer tiles (6 balanced the pairs' end times best: at 7 the
+// pairs without a boundary ended last).
+constexpr int kItemCost = 6;
 
 constexpr uint32_t kRankV = 0, kRankS = 1;
 constexpr uint16_t kMaskS = 1u << kRankS;
@@ -222,8 +228,11 @@ __device__ __forceinline__ bool wait_bar_warp(uint64_t *bar, uint32_t parity, vo
 }
 
 // The segments of one pair: consecutive (item, tile range) pieces of its
-// range [t_begin, t_end) of the global tile order, walked from item w0
-// (whose first tile has global index s0); tile counts come from seqlens.
+// range [t_begin, t_end) of the plan's order, walked from item w0 (whose
+// span starts at s0); tile counts come from seqlens.  In the plan's order an
+// item with n > 0 tiles spans kItemCost + n units, the first kItemCost
+// standing for its start-up cost and holding no tile: unit u of the span is
+// tile u - kItemCost.
 struct SegIter {
   const DecodeArgs *a;
   int W, t_begin, t_end, w, s;
@@ -240,16 +249,20 @@ struct SegIter {
     while (w < W && s < t_end) {
       bool bad = false;
       const int n = visible_len(*a, w, &bad);
-      const int st = s, e = s + (n + kTile - 1) / kTile;
+      const int nt = (n + kTile - 1) / kTile;
+      const int st = s, e = nt > 0 ? s + kItemCost + nt : s;
       const int cur = w++;
       s = e;
       if (e <= st || e <= t_begin) continue;
       const int g0 = st > t_begin ? st : t_begin;
       const int g1 = e < t_end ? e : t_end;
+      const int l0 = g0 - st - kItemCost > 0 ? g0 - st - kItemCost : 0;
+      const int l1 = g1 - st - kItemCost > 0 ? g1 - st - kItemCost : 0;
+      if (l1 <= l0) continue;  // only start-up units of this item here
       *item = cur;
-      *lt0 = g0 - st;
-      *lt1 = g1 - st;
-      *whole = (g0 == st) && (g1 == e);
+      *lt0 = l0;
+      *lt1 = l1;
+      *whole = (l0 == 0) && (l1 == nt);
       *n_vis = n;
       return true;
     }
@@ -367,7 +380,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       bool bad = false;
       const int n = visible_len(a, w, &bad);
       any_bad |= bad;
-      pre[w + 1] = (n + kTile - 1) / kTile;
+      const int nt = (n + kTile - 1) / kTile;
+      pre[w + 1] = nt > 0 ? nt + kItemCost : 0;
     }
     if (any_bad && pair == 0) set_device_error(a.err, kDevBounds);
     __syncthreads();
@@ -1052,9 +1066,11 @@ __global__ void __launch_bounds__(32 * kCombineRows) combine_tc_kernel(DecodeArg
   const int per = a.plan[0];
   const int s = a.plan[1 + w], e = a.plan[2 + w];
   if (e <= s || per <= 0) return;
-  const int p0 = s / per, p1 = (e - 1) / per;
+  // the item's tiles are units s + kItemCost .. e - 1 of the plan
+  const int f = s + kItemCost;
+  const int p0 = f / per, p1 = (e - 1) / per;
   if (p0 == p1) return;  // written directly by its pair
-  auto slot_of = [&](int p) { return 2 * p + ((s < p * per) ? 0 : 1); };
+  auto slot_of = [&](int p) { return 2 * p + ((f < p * per) ? 0 : 1); };
   // maximum and sum of exp(lse) over the pieces
   float mx = -INFINITY;
   bool poison = false;
