@@ -186,6 +186,8 @@ constexpr int kTraceTiles = 512, kTraceEvents = 8, kTracePairs = 2;
 __device__ unsigned long long g_trace[kTracePairs][2][kTraceEvents][kTraceTiles];
 // per CTA: kernel entry, range start (after setup), end of work
 __device__ unsigned long long g_trace_cta[2 * kMaxPairs][3];
+// first start and last end of the combine kernel's blocks
+__device__ unsigned long long g_trace_comb[2] = {~0ull, 0ull};
 #define MLA_TRACE_CTA(k) \
   do { if (threadIdx.x == 0) g_trace_cta[blockIdx.x][k] = ptx::globaltimer_ns(); } while (0)
 __device__ __forceinline__ void trace_ev(int pair, int npairs, uint32_t rank, int ev, int g) {
@@ -1058,6 +1060,15 @@ __global__ void __launch_bounds__(32 * kCombineRows) combine_tc_kernel(DecodeArg
   // launched early, behind the decode grid: its pieces are complete and
   // visible only after this wait
   ptx::grid_dependency_wait();
+#ifdef MLA_TRACE
+  if (threadIdx.x == 0) atomicMin(&g_trace_comb[0], ptx::globaltimer_ns());
+  struct CombEnd {
+    __device__ ~CombEnd() {
+      __syncthreads();
+      if (threadIdx.x == 0) atomicMax(&g_trace_comb[1], ptx::globaltimer_ns());
+    }
+  } comb_end;
+#endif
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long rowg = (long)blockIdx.x * kCombineRows + warp;
   const int W = a.B * a.Hq;
@@ -1163,10 +1174,13 @@ int pairs_for_device() {
 #ifdef MLA_TRACE
 extern "C" __attribute__((visibility("default"))) int mla_debug_read_trace(void *host,
                                                                           size_t bytes) {
-  if (bytes < sizeof(g_trace) + sizeof(g_trace_cta)) return -1;
+  if (bytes < sizeof(g_trace) + sizeof(g_trace_cta) + sizeof(g_trace_comb)) return -1;
   if (cudaMemcpyFromSymbol(host, g_trace, sizeof(g_trace)) != cudaSuccess) return -1;
-  return cudaMemcpyFromSymbol(static_cast<char *>(host) + sizeof(g_trace), g_trace_cta,
-                              sizeof(g_trace_cta)) == cudaSuccess ? 0 : -1;
+  if (cudaMemcpyFromSymbol(static_cast<char *>(host) + sizeof(g_trace), g_trace_cta,
+                           sizeof(g_trace_cta)) != cudaSuccess)
+    return -1;
+  return cudaMemcpyFromSymbol(static_cast<char *>(host) + sizeof(g_trace) + sizeof(g_trace_cta),
+                              g_trace_comb, sizeof(g_trace_comb)) == cudaSuccess ? 0 : -1;
 }
 #endif
 
@@ -1227,6 +1241,12 @@ cudaError_t launch_decode_tc(const void *q_lat, const void *q_rope, const void *
   a.o_part = o_part;
   a.lse_part = reinterpret_cast<float *>(ws + kWsHeader + part_bytes());
   a.plan = reinterpret_cast<int *>(ws + kWsHeader + part_bytes() + lse_part_bytes());
+#ifdef MLA_TRACE
+  {
+    const unsigned long long init[2] = {~0ull, 0ull};
+    cudaMemcpyToSymbolAsync(g_trace_comb, init, sizeof(init), 0, cudaMemcpyHostToDevice, st);
+  }
+#endif
   // both kernels are programmatic dependents of their predecessor in the
   // stream (each waits on it in-kernel before reading its outputs)
   cudaLaunchAttribute pdl[1];
