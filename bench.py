@@ -51,6 +51,25 @@ def visible_tokens(seqlens, Hq):
     return int(sum(np.maximum(0, s - Hq + i + 1).sum() for i in range(Hq)))
 
 
+def max_over_ranks(values, world, device=None):
+    """The element-wise maximum of ``values`` over all ranks (the slowest
+    replica sets the whole job's time).  NCCL reduces device tensors, gloo
+    host tensors."""
+    if world <= 1:
+        return [float(v) for v in values]
+    on_dev = device is not None and torch.distributed.get_backend() == "nccl"
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64,
+                     device=device if on_dev else "cpu")
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return t.cpu().tolist()
+
+
+def whole_job_rate(work_per_rank, world, ms):
+    """Throughput of ``world`` replicas that each did ``work_per_rank`` units,
+    the slowest in ``ms`` milliseconds (weak scaling): units per second."""
+    return world * work_per_rank / (ms * 1e-3)
+
+
 def decode_work(w, seqlens):
     """FLOPs and bytes of mla_decode: QK^T over d_c + d_r and P C over d_c
     per visible (token, query slot) and head; bytes are the cache rows read
@@ -248,13 +267,8 @@ def run_ours(args, rank, world, device):
     qproj = measure_project_query(mla, args, w, dev, dims, flush, stream, device)
 
     # ---- reduce over ranks ----------------------------------------------------
-    t_step = float(np.mean(step_ms))
-    t_dec = float(np.mean(dec_ms))
-    t_e2e = float(np.mean(e2e_ms))
-    if world > 1:
-        t = torch.tensor([t_step, t_dec, t_e2e], dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        t_step, t_dec, t_e2e = t.tolist()
+    t_step, t_dec, t_e2e = max_over_ranks(
+        [float(np.mean(step_ms)), float(np.mean(dec_ms)), float(np.mean(e2e_ms))], world, device)
     if rank != 0:
         return None
 
@@ -270,7 +284,7 @@ def run_ours(args, rank, world, device):
     bound = "hbm" if dbytes / (hbm * 1e9) >= dflops / (tc_burst * 1e12) else "tensor"
     achieved, peak, unit = (dec_gbs, hbm, "GB/s") if bound == "hbm" else (dec_tflops, tc_burst,
                                                                          "TFLOP/s")
-    value = world * step_flops / (t_step * 1e-3) / 1e12
+    value = whole_job_rate(step_flops, world, t_step) / 1e12
     launches_per_step = 1 + 1 + decode_launches(mla, dims, w) + 1
     traffic = load_traffic(args.workload)
     res = {
@@ -320,7 +334,7 @@ def run_ours(args, rank, world, device):
             "traffic": traffic,
         },
         "e2e": {
-            "value": round(world * step_flops / (t_e2e * 1e-3) / 1e12, 3),
+            "value": round(whole_job_rate(step_flops, world, t_e2e) / 1e12, 3),
             "unit": "TFLOP/s",
             "ms_per_step": round(t_e2e, 5),
             "h2d_bytes_per_step": int(h2d),
