@@ -73,19 +73,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Cluster-scope acquire variant (pairs with mbar_arrive_remote).
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n"
-      " mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
 // Non-suspending probe, cluster-scope acquire.  Waits on barriers that
 // another CTA of the cluster arrives on poll with this instead of try_wait:
 // a thread suspended in try_wait can be woken late by a remote arrival.
@@ -168,18 +155,6 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n"
                "barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// Store 4 floats into the same shared-memory offset of CTA `cta_rank`.
-__device__ __forceinline__ void st_cluster_v4(const void *local_ptr, uint32_t cta_rank, float a,
-                                              float b, float c, float d) {
-  uint32_t remote;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
-               : "=r"(remote)
-               : "r"(smem_u32(local_ptr)), "r"(cta_rank));
-  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(remote), "f"(a), "f"(b),
-               "f"(c), "f"(d)
-               : "memory");
 }
 
 // ---- tcgen05 ------------------------------------------------------------------------
@@ -269,7 +244,7 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// ---- cluster: multicast copies, remote stores and loads --------------------------
+// ---- cluster stores and loads, TMEM-operand MMA, conversions ---------------------
 
 // Shared::cluster address of the same shared-memory offset in CTA `cta_rank`.
 __device__ __forceinline__ uint32_t map_to_rank(const void *local_ptr, uint32_t cta_rank) {
@@ -278,32 +253,6 @@ __device__ __forceinline__ uint32_t map_to_rank(const void *local_ptr, uint32_t 
                : "=r"(remote)
                : "r"(smem_u32(local_ptr)), "r"(cta_rank));
   return remote;
-}
-
-// TMA load delivered to the same offset in every CTA of `cta_mask`; each
-// destination CTA's mbarrier at `bar`'s offset receives the byte count.
-__device__ __forceinline__ void tma_load_2d_mc(void *dst, const CUtensorMap *map, uint64_t *bar,
-                                               int x, int y, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "h"(cta_mask)
-      : "memory");
-}
-
-// Fetch one tensor-map box into L2 (no shared-memory destination).
-__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int x, int y) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global [%0, {%1, %2}];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(x), "r"(y)
-               : "memory");
-}
-
-// Fetch `bytes` (a multiple of 16) of global memory into L2.
-__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)),
-               "r"(bytes)
-               : "memory");
 }
 
 // Asynchronous 16-byte / 4-byte store into another CTA's shared memory; the
@@ -334,67 +283,6 @@ __device__ __forceinline__ int ld_cluster_s32(uint32_t addr) {
 
 __device__ __forceinline__ void st_cluster_s32(uint32_t addr, int v) {
   asm volatile("st.shared::cluster.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
-
-// Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned)
-// from this CTA's shared memory into another CTA's shared memory; the
-// mbarrier at `remote_bar` (in the destination CTA) receives the bytes.
-// The copy reads its source through the async proxy: generic-proxy writes of
-// the source need fence_proxy_async_smem() first.
-__device__ __forceinline__ void bulk_copy_to_peer(uint32_t remote_dst, const void *local_src,
-                                                  uint32_t bytes, uint32_t remote_bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
-      "[%3];" ::"r"(remote_dst),
-      "r"(smem_u32(local_src)), "r"(bytes), "r"(remote_bar)
-      : "memory");
-}
-
-// Bulk copy of `bytes` (multiple of 16, 16-byte aligned) from global memory
-// into this CTA's shared memory, counted on `bar`.
-__device__ __forceinline__ void bulk_load_global(void *dst, const void *src, uint32_t bytes,
-                                                 uint64_t *bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
-
-// TMA store of one tensor-map box from this CTA's shared memory (bulk group).
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void *src, int x,
-                                             int y) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
-          reinterpret_cast<uint64_t>(map)),
-      "r"(smem_u32(src)), "r"(x), "r"(y)
-      : "memory");
-}
-
-// Make generic-proxy global writes visible to the async proxy (a later bulk
-// copy or TMA that reads them).
-__device__ __forceinline__ void fence_proxy_async_global() {
-  asm volatile("fence.proxy.async.global;" ::: "memory");
-}
-
-__device__ __forceinline__ void bulk_commit_group() {
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-
-// Wait until every bulk copy this thread committed has finished reading its
-// source (the copies themselves may still be in flight).
-__device__ __forceinline__ void bulk_wait_read_all() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-
-// Wait until every bulk copy this thread committed has completed.
-__device__ __forceinline__ void bulk_wait_all() {
-  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
-
-// Arrive (with an expected byte count) on this CTA's mbarrier, no return value.
-__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
-  mbar_arrive_expect_tx(bar, bytes);
 }
 
 // D[tmem] (+)= A[tmem] * B[smem]^T (A read from tensor memory, K-major: one
