@@ -1082,6 +1082,43 @@ __global__ void __launch_bounds__(32 * kCombineRows) combine_tc_kernel(DecodeArg
   const int p0 = f / per, p1 = (e - 1) / per;
   if (p0 == p1) return;  // written directly by its pair
   auto slot_of = [&](int p) { return 2 * p + ((f < p * per) ? 0 : 1); };
+  __nv_bfloat16 *dst = a.o_lat + (size_t)rowg * kDc;
+  if (p1 == p0 + 1) {
+    // two pieces (an item cut once): every load in flight at once
+    const int s0 = slot_of(p0), s1 = slot_of(p1);
+    const float l0 = a.lse_part[(size_t)s0 * 128 + h], l1 = a.lse_part[(size_t)s1 * 128 + h];
+    const float4 *src0 =
+        reinterpret_cast<const float4 *>(a.o_part + ((size_t)s0 * 128 + h) * kDc) + lane * 4;
+    const float4 *src1 =
+        reinterpret_cast<const float4 *>(a.o_part + ((size_t)s1 * 128 + h) * kDc) + lane * 4;
+    float4 v0[4], v1[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      v0[q] = src0[q];
+      v1[q] = src1[q];
+    }
+    const float mx2 = fmaxf(l0, l1);
+    if (isnan(l0) || isnan(l1) || mx2 == -INFINITY) {
+      reinterpret_cast<uint4 *>(dst)[lane] = make_uint4(0, 0, 0, 0);
+      reinterpret_cast<uint4 *>(dst)[lane + 32] = make_uint4(0, 0, 0, 0);
+      if (lane == 0) a.lse[rowg] = -INFINITY;
+      return;
+    }
+    const float w0 = expf(l0 - mx2), w1 = expf(l1 - mx2);
+    const float inv2 = 1.f / (w0 + w1), a0 = w0 * inv2, a1 = w1 * inv2;
+    uint32_t pk[8];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      pk[2 * q] = ptx::pack_bf16x2(fmaf(a1, v1[q].x, a0 * v0[q].x), fmaf(a1, v1[q].y, a0 * v0[q].y));
+      pk[2 * q + 1] =
+          ptx::pack_bf16x2(fmaf(a1, v1[q].z, a0 * v0[q].z), fmaf(a1, v1[q].w, a0 * v0[q].w));
+    }
+    uint4 *d4 = reinterpret_cast<uint4 *>(dst) + lane * 2;
+    d4[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    d4[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+    if (lane == 0) a.lse[rowg] = mx2 + logf(w0 + w1);
+    return;
+  }
   // maximum and sum of exp(lse) over the pieces
   float mx = -INFINITY;
   bool poison = false;
@@ -1093,7 +1130,6 @@ __global__ void __launch_bounds__(32 * kCombineRows) combine_tc_kernel(DecodeArg
 #pragma unroll
   for (int off = 16; off; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
   poison = __any_sync(0xffffffffu, poison);
-  __nv_bfloat16 *dst = a.o_lat + (size_t)rowg * kDc;
   if (poison || mx == -INFINITY) {
     reinterpret_cast<uint4 *>(dst)[lane] = make_uint4(0, 0, 0, 0);
     reinterpret_cast<uint4 *>(dst)[lane + 32] = make_uint4(0, 0, 0, 0);
