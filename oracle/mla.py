@@ -23,7 +23,7 @@ cached token it rebuilds the per-head key ``K_j = W_UK[h] c_j`` and value
 an exact identity ("Mathematical Prerequisites for DeepSeek-V2" sections 6
 and 7), so the absorbed GPU path must agree with this up to rounding.
 
-Readings of points the pages leave open (each listed in the design doc):
+Readings of points the pages leave open:
 
 * ``seqlens[b]`` counts cached tokens *after* the ``Hq`` current tokens have
   been appended; query slot ``i`` of ``Hq`` sees positions

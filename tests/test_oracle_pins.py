@@ -91,7 +91,8 @@ def test_prereq_running_example():
 
 
 def p5_library_layout(g):
-    """The worked example in the library's layout (see the design doc readings).
+    """The worked example in the library's layout (W_UK, W_UV transposed into
+    [H, d_h, d_c]).
 
     Returns q_nope [1,1,H,d_h], q_rope [1,1,H,d_r], cache [1,4,d_c+d_r],
     block_table [[0]], seqlens [4], W_UK / W_UV [H,d_h,d_c].
