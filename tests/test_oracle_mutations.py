@@ -16,7 +16,8 @@ from oracle import mla, upstream
 import test_oracle_pins as pins
 
 ALL_PINS = (pins.check_prereq, pins.check_p5_upstream, pins.check_p5_content_path,
-            pins.check_p5_norope_decode, pins.check_p5_full_decode)
+            pins.check_p5_norope_decode, pins.check_p5_full_decode,
+            pins.check_projection_layouts)
 
 
 def _some_pin_fails():
@@ -77,6 +78,37 @@ def _attention_row_lse_without_max(q_nope, q_rope, rows, W_UK_h, W_UV_h, scale, 
 
 _ORIG_ROW = mla.attention_row
 
+
+def _cache_row_unrotated(h_t, W_DKV, W_KR, position, theta):  # k_R cached before RoPE
+    return np.concatenate([upstream.down_project(W_DKV, h_t), mla.project(W_KR, h_t)])
+
+
+def _cache_row_rope_on_latent(h_t, W_DKV, W_KR, position, theta):  # rotates the wrong part
+    c = upstream.down_project(W_DKV, h_t)
+    k = mla.project(W_KR, h_t)
+    return np.concatenate([upstream.rope(c, position, np.resize(theta, c.size // 2)), k])
+
+
+def _query_rope_across_heads(h_t, W_Q, W_QR, H, d_h, d_r, position, theta):
+    # all heads' RoPE parts rotated as one vector (frequencies of H*d_r)
+    q = mla.project(W_Q, h_t).reshape(H, d_h)
+    qr = mla.project(W_QR, h_t)
+    th = upstream.rope_frequencies(H * d_r) * float(np.asarray(theta).ravel()[0])
+    return q, upstream.rope(qr, position, th).reshape(H, d_r)
+
+
+def _query_heads_interleaved(h_t, W_Q, W_QR, H, d_h, d_r, position, theta):
+    # head h taken as every H-th coordinate instead of a contiguous slice
+    q = mla.project(W_Q, h_t).reshape(d_h, H).T
+    qr = mla.project(W_QR, h_t)
+    return q, np.stack([upstream.rope(qr[i * d_r:(i + 1) * d_r], position, theta)
+                        for i in range(H)])
+
+
+def _output_projection_transposed(out, W_O):  # heads concatenated in the wrong order
+    o = np.asarray(out, np.float64)
+    return o.T.reshape(-1) @ np.asarray(W_O, np.float64)
+
 MUTATIONS = {
     "project transposed": (mla, "project", _wrong_project),
     "keys use W_UK^T": (mla, "reconstruct_keys", _keys_transposed),
@@ -87,6 +119,11 @@ MUTATIONS = {
     "RoPE wrong sign": (upstream, "rope", _rope_wrong_sign),
     "RoPE term dropped": (mla, "attention_row", _attention_row_no_rope_term),
     "lse drops the max": (mla, "attention_row", _attention_row_lse_without_max),
+    "cache row k_R not rotated": (upstream, "cache_row", _cache_row_unrotated),
+    "cache row rotates the latent": (upstream, "cache_row", _cache_row_rope_on_latent),
+    "query RoPE across heads": (upstream, "query_projection", _query_rope_across_heads),
+    "query heads interleaved": (upstream, "query_projection", _query_heads_interleaved),
+    "W_O heads in wrong order": (mla, "output_projection", _output_projection_transposed),
 }
 
 

@@ -221,6 +221,33 @@ def check_p5_full_decode():
     _close(mla.out_proj(o_lat, W_UV), out, 1e-12, "W_UV o_lat == sum p V")
 
 
+def check_projection_layouts():
+    """Special cases that fix the head and row layouts of the projections
+    (the worked example cannot: its query [1, 2, 2, 1] reads the same with
+    heads taken contiguously or interleaved).  With identity weights and
+    position 0 (no rotation), head h of the query must be coordinates
+    h*d_h .. h*d_h+d_h-1 of the hidden state, and the cache row is the hidden
+    state itself; at position 1 with theta = pi/2 each RoPE pair (x0, x1)
+    becomes (-x1, x0) ("MLA, dim by dim" 3: adjacent pairs)."""
+    H, d_h, d_r = 3, 4, 2
+    h = np.arange(1.0, 1.0 + H * d_h)
+    qn, qr = upstream.query_projection(h, np.eye(H * d_h), np.eye(H * d_r, H * d_h), H, d_h,
+                                       d_r, 0, np.array([0.3]))
+    _close(qn, h.reshape(H, d_h), EXACT, "query heads are contiguous slices")
+    _close(qr, h[:H * d_r].reshape(H, d_r), EXACT, "RoPE query heads are contiguous slices")
+    _, qr1 = upstream.query_projection(h, np.eye(H * d_h), np.eye(H * d_r, H * d_h), H, d_h, d_r,
+                                       1, np.array([math.pi / 2]))
+    want = np.stack([[-h[2 * i + 1], h[2 * i]] for i in range(H)])
+    _close(qr1, want, 1e-12, "each head's RoPE pair turns by 90 degrees")
+    x = np.arange(1.0, 7.0)
+    row = upstream.cache_row(x, np.eye(4, 6), np.eye(2, 6, k=4), 0, np.array([0.3]))
+    _close(row, x, EXACT, "cache row [c ; k_R] in order")
+
+
+def test_projection_layouts():
+    check_projection_layouts()
+
+
 def test_p5_upstream_and_rope():
     check_p5_upstream()
 
