@@ -252,7 +252,10 @@ mla_status mla_decode(const void *q_lat, const void *q_rope, const void *cache,
 mla_status mla_out_proj(const void *o_lat, const void *W_UV, void *out, int B,
                         int Hq, const mla_dims *dims, mla_stream_t stream);
 
-/* Synchronise `stream`, read and clear the workspace's device error word.
+/* Synchronise `stream`, read and clear the workspace's device error word,
+ * together with the library-wide word of the tensor-core GEMMs
+ * (mla_absorb_query, mla_out_proj, mla_project_append, mla_project_query,
+ * mla_o_proj), whose bounded waits record MLA_ERR_TIMEOUT there.
  * Returns MLA_OK, MLA_ERR_DEVICE_BOUNDS, MLA_ERR_TIMEOUT or MLA_ERR_CUDA. */
 mla_status mla_get_error(void *workspace, mla_stream_t stream);
 
