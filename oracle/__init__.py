@@ -9,6 +9,8 @@ Modules
 -------
 ``oracle.mla``         the decode step written out as its plain definition
                        (un-absorbed: K and V are reconstructed per cached token)
+``oracle.prefill``     prefill in the standard order: K and V rebuilt from the
+                       latents, then causal attention over d_k and d_v
 ``oracle.upstream``    down-projection and RoPE, used only to synthesise the
                        inputs of the tiny fp32 workload
 ``oracle.accounting``  closed-form cache sizes and FLOP counts
@@ -17,4 +19,4 @@ Every function is pinned by ``tests/test_oracle_*.py`` to numbers the pages
 print, to closed forms, or to textbook special cases.
 """
 
-from . import accounting, mla, upstream  # noqa: F401
+from . import accounting, mla, prefill, upstream  # noqa: F401

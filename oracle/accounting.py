@@ -57,3 +57,13 @@ def decode_tensor_flops_per_token(H, d_c, d_r):
     """Tensor-core FLOPs of the hot loop per visible token and query slot:
     ``QK^T`` over ``d_c + d_r`` plus ``P C`` over ``d_c`` (no score add)."""
     return contraction_flops([H], d_c + d_r) + contraction_flops([H, d_c], 1)
+
+
+def prefill_attention_flops(T, H, d_qk, d_v, causal=True):
+    """Tensor FLOPs of the prefill core attention of one ``T``-token sequence
+    ("MLA, dim by dim" 4.1: ``S = Q K^T`` contracts ``d_qk``, ``O = P V``
+    contracts the key axis into ``d_v``).  Dense, that is the pages'
+    ``2 h T^2 (d_k + d_v)``; causal, only the ``T (T + 1) / 2`` visible
+    (query, key) pairs count."""
+    pairs = T * (T + 1) // 2 if causal else T * T
+    return 2 * H * (d_qk + d_v) * pairs

@@ -288,3 +288,25 @@ def query_tensors(seed, B, Hq, H, d_h, d_r, d_model):
         "W_Q": _normal(g, (H * d_h, d_model), std=wstd),
         "W_QR": _normal(g, (H * d_r, d_model), std=wstd),
     }
+
+
+def prefill_tensors(seed, seqlens, H, d_h=128, d_c=512, d_r=64):
+    """Inputs of a packed prefill: sequences of the given lengths laid end to
+    end (``cu_seqlens`` [B+1] int32, the prefix sums), ``q_nope [T, H, d_h]``,
+    ``q_rope [T, H, d_r]``, ``c_kv [T, d_c]``, ``k_r [T, d_r]`` ``~ N(0,1)``
+    and ``W_UK, W_UV [H, d_h, d_c] ~ N(0, 1/d_c)`` (the decode recipe, so
+    scaled scores have unit variance).  bf16."""
+    g = _gen(seed)
+    cu = np.zeros(len(seqlens) + 1, dtype=np.int32)
+    cu[1:] = np.cumsum(np.asarray(seqlens, dtype=np.int64))
+    T = int(cu[-1])
+    wstd = 1.0 / math.sqrt(d_c)
+    return {
+        "cu_seqlens": torch.from_numpy(cu),
+        "q_nope": _normal(g, (T, H, d_h)),
+        "q_rope": _normal(g, (T, H, d_r)),
+        "c_kv": _normal(g, (T, d_c)),
+        "k_r": _normal(g, (T, d_r)),
+        "W_UK": _normal(g, (H, d_h, d_c), std=wstd),
+        "W_UV": _normal(g, (H, d_h, d_c), std=wstd),
+    }
