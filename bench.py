@@ -265,6 +265,7 @@ def run_ours(args, rank, world, device):
     proj = measure_project_append(mla, args, w, dev, inp, dims, flush, stream, device)
     oproj = measure_o_proj(mla, args, w, out, dims, flush, stream, device)
     qproj = measure_project_query(mla, args, w, dev, dims, flush, stream, device)
+    pre = measure_prefill(mla, args, w, flush, stream, device)
 
     # ---- reduce over ranks ----------------------------------------------------
     t_step, t_dec, t_e2e = max_over_ranks(
@@ -350,6 +351,8 @@ def run_ours(args, rank, world, device):
         res["o_proj"] = oproj
     if qproj is not None:
         res["project_query"] = qproj
+    if pre is not None:
+        res["prefill"] = pre
     return res
 
 
@@ -436,6 +439,47 @@ def measure_o_proj(mla, args, w, out, dims, flush, stream, device):
         "gbs": round(gbs, 1),
         "tflops": round(flops / (ms * 1e-3) / 1e12, 2),
         "hbm_frac": round(gbs / peaks["hbm_gbs"], 4),
+        "launches": 2,
+    }
+
+
+# prompts of the prefill measurement: four 4096-token sequences, packed
+PREFILL_SEQLENS = [4096] * 4
+
+
+def measure_prefill(mla, args, w, flush, stream, device):
+    """``mla_prefill`` (standard order: K and V rebuilt by one GEMM, then
+    causal attention) on four 4096-token prompts with the workload's heads.
+    Algorithmic FLOPs: the rebuild ``2 T H (d_h + d_h) d_c`` plus the
+    attention's ``2 H (d_h + d_r + d_h)`` per visible (query, key) pair,
+    ``T_b (T_b + 1) / 2`` pairs per prompt; both are tensor-core work, so the
+    fraction is taken of the measured dense bf16 peak."""
+    if w.dtype != "bf16" or (w.d_h, w.d_c, w.d_r) != (128, 512, 64):
+        return None
+    t = {k: v.to(device) for k, v in synth.prefill_tensors(w.seed + 400, PREFILL_SEQLENS,
+                                                            w.H).items()}
+    T = sum(PREFILL_SEQLENS)
+    dims = mla.Dims(H=w.H, d_h=128, d_c=512, d_r=64, block_size=64, dtype=torch.bfloat16)
+    out = torch.empty(T, w.H, 128, dtype=torch.bfloat16, device=device)
+    lse = torch.empty(T, w.H, dtype=torch.float32, device=device)
+    ws = torch.zeros(mla.mla_prefill_workspace_size(T, dims), dtype=torch.uint8, device=device)
+    ms = _time_calls(lambda: mla.mla_prefill(t["q_nope"], t["q_rope"], t["c_kv"], t["k_r"],
+                                             t["W_UK"], t["W_UV"], t["cu_seqlens"],
+                                             max(PREFILL_SEQLENS), dims, out, lse, ws,
+                                             stream=stream),
+                     max(3, min(args.steps, 20)), flush, stream)
+    kv_flops = 2 * T * w.H * 256 * 512
+    attn_flops = sum(n * (n + 1) // 2 for n in PREFILL_SEQLENS) * 2 * w.H * (128 + 64 + 128)
+    peaks, _ = load_peaks()
+    tflops = (kv_flops + attn_flops) / (ms * 1e-3) / 1e12
+    return {
+        "ms": round(ms, 5),
+        "prompts": PREFILL_SEQLENS,
+        "H": w.H,
+        "kv_rebuild_flops": kv_flops,
+        "attention_flops": attn_flops,
+        "tflops": round(tflops, 1),
+        "tensor_frac_of_burst": round(tflops / peaks["bf16_tflops"], 4),
         "launches": 2,
     }
 

@@ -16,6 +16,8 @@
  * mla_project_append can replace mla_append_cache when the caller holds the
  * new tokens' hidden states: it computes c = W_DKV h and k_R = RoPE(W_KR h)
  * and writes them straight into the cache.
+ * mla_prefill runs attention for whole prompts in the standard (un-absorbed)
+ * order, the one that is cheaper when every token is a query.
  *
  * The per-head keys W_UK c_j and values W_UV c_j of cached tokens are never
  * formed.  Sources (page title, section):
@@ -252,10 +254,55 @@ mla_status mla_decode(const void *q_lat, const void *q_rope, const void *cache,
 mla_status mla_out_proj(const void *o_lat, const void *W_UV, void *out, int B,
                         int Hq, const mla_dims *dims, mla_stream_t stream);
 
+/* Bytes of device workspace mla_prefill needs: the error word plus the
+ * rebuilt keys and values, 512 bytes per (token, head) in bf16 (about
+ * 268 MB for 4096 tokens at H = 128).  Returns MLA_ERR_UNSUPPORTED for
+ * shapes mla_prefill does not take. */
+mla_status mla_prefill_workspace_size(int total_tokens, const mla_dims *dims,
+                                      size_t *bytes);
+
+/* MLA prefill in the standard order ("MLA, dim by dim" 4.1; "MLA
+ * Explained", training and prefill): the per-head keys and values are
+ * rebuilt from the latents first, then causal attention runs over
+ * d_k = d_h + d_r and d_v = d_h (absorption would put the T^2 contractions
+ * on d_c instead).  Sequences are packed end to end: sequence b is tokens
+ * cu_seqlens[b] .. cu_seqlens[b+1]-1, and token t of it (0-based) attends to
+ * tokens 0..t of the same sequence.  For every such token t and head h:
+ *   K_j = [W_UK[h] c_j ; kR_j],  V_j = W_UV[h] c_j
+ *   s_j = [q_nope[t,h,:] ; q_rope[t,h,:]] . K_j * scale,  j <= t
+ *   out[t,h,:] = sum_j softmax_j(s_j) V_j,   lse[t,h] = ln sum_j exp(s_j)
+ * (scores as in mla_decode, so a sequence's last row equals a decode of it).
+ *   q_nope      [total_tokens, H, d_h]             input
+ *   q_rope      [total_tokens, H, d_r] (rotated)   input
+ *   c_kv        [total_tokens, d_c]                input
+ *   k_r         [total_tokens, d_r]   (rotated)    input
+ *   W_UK, W_UV  [H, d_h, d_c]                      input
+ *   cu_seqlens  [B + 1] int32, cu_seqlens[0] = 0, non-decreasing,
+ *               cu_seqlens[B] = total_tokens       input (device)
+ *   max_seqlen  >= every sequence length (sizes the grid)
+ *   out         [total_tokens, H, d_h]             output
+ *   lse         [total_tokens, H] float32          output
+ *   workspace   >= mla_prefill_workspace_size bytes, 256-byte aligned; its
+ *               first word is the error word that mla_get_error reads
+ * Supported: bf16, d_h = 128, d_c = 512, d_r = 64 (else MLA_ERR_UNSUPPORTED);
+ * B <= 65535.  K and V are rounded to bf16 once after their fp32
+ * accumulation; scores and the softmax are fp32, P is rounded to bf16 for
+ * the P V product, out is rounded to bf16 once.  A sequence whose
+ * cu_seqlens entries are out of range (negative length, longer than
+ * max_seqlen, past total_tokens) is skipped: its rows are not written and
+ * MLA_ERR_DEVICE_BOUNDS is recorded in the error word. */
+mla_status mla_prefill(const void *q_nope, const void *q_rope, const void *c_kv,
+                       const void *k_r, const void *W_UK, const void *W_UV,
+                       const int32_t *cu_seqlens, int B, int max_seqlen,
+                       int total_tokens, const mla_dims *dims, void *out,
+                       float *lse, void *workspace, size_t workspace_bytes,
+                       mla_stream_t stream);
+
 /* Synchronise `stream`, read and clear the workspace's device error word,
  * together with the library-wide word of the tensor-core GEMMs
  * (mla_absorb_query, mla_out_proj, mla_project_append, mla_project_query,
- * mla_o_proj), whose bounded waits record MLA_ERR_TIMEOUT there.
+ * mla_o_proj, and the key / value rebuild of mla_prefill), whose bounded
+ * waits record MLA_ERR_TIMEOUT there.
  * Returns MLA_OK, MLA_ERR_DEVICE_BOUNDS, MLA_ERR_TIMEOUT or MLA_ERR_CUDA. */
 mla_status mla_get_error(void *workspace, mla_stream_t stream);
 

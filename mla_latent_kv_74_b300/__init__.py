@@ -55,6 +55,8 @@ EXPORTED = (
     "mla_o_proj",
     "mla_project_query_workspace_size",
     "mla_project_query",
+    "mla_prefill_workspace_size",
+    "mla_prefill",
 )
 
 # size of the scratch array built into the library for mla_decode_noalloc
@@ -106,6 +108,8 @@ def _load():
         "mla_o_proj": [P, P, P, I, I, I, D, P, Z, P],
         "mla_project_query_workspace_size": [I, I, I, D, ctypes.POINTER(Z)],
         "mla_project_query": [P, P, P, I, ctypes.c_float, P, I, I, D, P, P, P, Z, P],
+        "mla_prefill_workspace_size": [I, D, ctypes.POINTER(Z)],
+        "mla_prefill": [P, P, P, P, P, P, P, I, I, I, D, P, P, P, Z, P],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -263,6 +267,27 @@ def mla_decode_noalloc(q_lat, q_rope, cache, num_blocks, block_table, seqlens, m
                                    _ptr(block_table), block_table.shape[1], _ptr(seqlens),
                                    int(max_seqlen), B, Hq, ctypes.byref(dims), _ptr(o_lat),
                                    _ptr(lse), _stream(stream)), "mla_decode_noalloc")
+
+
+def mla_prefill_workspace_size(total_tokens, dims: Dims) -> int:
+    n = ctypes.c_size_t(0)
+    _check(_lib.mla_prefill_workspace_size(int(total_tokens), ctypes.byref(dims),
+                                           ctypes.byref(n)), "mla_prefill_workspace_size")
+    return n.value
+
+
+def mla_prefill(q_nope, q_rope, c_kv, k_r, W_UK, W_UV, cu_seqlens, max_seqlen, dims: Dims,
+                out, lse, workspace, stream=None):
+    """Causal MLA prefill of packed sequences in the standard order (K and V
+    rebuilt from the latents, attention over d_h + d_r and d_h):
+    q_nope [T,H,d_h], q_rope [T,H,d_r], c_kv [T,d_c], k_r [T,d_r],
+    cu_seqlens [B+1] int32 on the device -> out [T,H,d_h], lse [T,H]."""
+    _check(_lib.mla_prefill(_ptr(q_nope), _ptr(q_rope), _ptr(c_kv), _ptr(k_r), _ptr(W_UK),
+                            _ptr(W_UV), _ptr(cu_seqlens), cu_seqlens.shape[0] - 1,
+                            int(max_seqlen), q_nope.shape[0], ctypes.byref(dims), _ptr(out),
+                            _ptr(lse), _ptr(workspace),
+                            workspace.numel() * workspace.element_size(), _stream(stream)),
+           "mla_prefill")
 
 
 def mla_get_error(workspace, stream=None) -> int:

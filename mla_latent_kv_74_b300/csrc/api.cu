@@ -225,6 +225,40 @@ MLA_API mla_status mla_decode(const void *q_lat, const void *q_rope, const void 
                                         o_lat, lse, workspace, st));
 }
 
+MLA_API mla_status mla_prefill_workspace_size(int total_tokens, const mla_dims *dims,
+                                              size_t *bytes) {
+  if (!bytes) return MLA_ERR_INVALID_ARG;
+  if (!dims_ok(dims)) return dims ? MLA_ERR_UNSUPPORTED : MLA_ERR_INVALID_ARG;
+  if (total_tokens < 0) return MLA_ERR_INVALID_ARG;
+  if (!tc_prefill_supported(*dims)) return MLA_ERR_UNSUPPORTED;
+  *bytes = prefill_workspace_bytes(total_tokens, *dims);
+  return MLA_OK;
+}
+
+MLA_API mla_status mla_prefill(const void *q_nope, const void *q_rope, const void *c_kv,
+                               const void *k_r, const void *W_UK, const void *W_UV,
+                               const int32_t *cu_seqlens, int B, int max_seqlen,
+                               int total_tokens, const mla_dims *dims, void *out, float *lse,
+                               void *workspace, size_t workspace_bytes, mla_stream_t stream) {
+  if (!dims_ok(dims)) return dims ? MLA_ERR_UNSUPPORTED : MLA_ERR_INVALID_ARG;
+  if (B < 0 || B > 65535 || max_seqlen < 0 || total_tokens < 0) return MLA_ERR_INVALID_ARG;
+  if ((max_seqlen + 127) / 128 > 65535) return MLA_ERR_INVALID_ARG;
+  if (!tc_prefill_supported(*dims)) return MLA_ERR_UNSUPPORTED;
+  if (B == 0 || total_tokens == 0) return MLA_OK;
+  if (max_seqlen == 0) return MLA_ERR_INVALID_ARG;  // tokens, but no sequence may hold one
+  if (!q_nope || !q_rope || !c_kv || !k_r || !W_UK || !W_UV || !cu_seqlens || !out || !lse)
+    return MLA_ERR_INVALID_ARG;
+  if (!al(q_nope, 16) || !al(q_rope, 16) || !al(c_kv, 16) || !al(k_r, 16) || !al(W_UK, 16) ||
+      !al(W_UV, 16) || !al(cu_seqlens, 4) || !al(out, 16) || !al(lse, 4))
+    return MLA_ERR_INVALID_ARG;
+  if (!workspace || !al(workspace, 256) ||
+      workspace_bytes < prefill_workspace_bytes(total_tokens, *dims))
+    return MLA_ERR_WORKSPACE;
+  return cuda_status(launch_prefill_tc(q_nope, q_rope, c_kv, k_r, W_UK, W_UV, cu_seqlens, B,
+                                       max_seqlen, total_tokens, *dims, eff_scale(dims), out,
+                                       lse, workspace, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 MLA_API mla_status mla_get_error(void *workspace, mla_stream_t stream) {
   if (!workspace || !al(workspace, 256)) return MLA_ERR_WORKSPACE;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

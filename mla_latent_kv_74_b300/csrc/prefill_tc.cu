@@ -1,0 +1,412 @@
+// MLA prefill in the standard order on the 5th-generation tensor cores
+// (sm_103a): keys and values are rebuilt from the latents first, then causal
+// attention runs over d_k = d_h + d_r and d_v = d_h.
+//
+// Math ("MLA, dim by dim" 4.1; "MLA Explained", training and prefill): per
+// packed sequence and head h,
+//   K = [C W_UK[h]^T ; k_R]   (T x 192),   V = C W_UV[h]^T   (T x 128)
+//   S = [q_nope ; q_rope] K^T * scale,   causal row softmax,   out = P V
+// with lse the natural log-sum-exp of the scaled scores.  Absorbing W_UK and
+// W_UV here would move the T^2 contractions from 192 / 128 onto d_c = 512,
+// so unlike decode the up-projections run first: one tensor-core GEMM writes
+// [K_nope | V] per (token, head) into the workspace (head_gemm_kernel), and
+// this kernel reads it.
+//
+// One CTA per (head, sequence, 128-query tile), heaviest query tiles first.
+// Queries are the MMA M dimension (128 rows = TMEM lanes), keys come in
+// tiles of 128:
+//   S  = Q K^T    M=128, N=128, K=192  A = Q (smem), B = K tile (smem)
+//   O += P V      M=128, N=128, K=128  A = P (TMEM, bf16), B = V tile (smem,
+//                                       MN-major)
+// TMEM (512 columns): two 128-column score buffers, the 128-column output
+// accumulator, two 64-column buffers of packed bf16 probabilities.  Shared
+// memory: the query tile (48 KB) and two stages each of K (48 KB) and V
+// (32 KB) tiles, all 128-byte swizzled, loaded by TMA.
+//
+// Warp roles (192 threads): warp 0 issues TMA, warp 1 owns TMEM and issues
+// MMAs, warps 2-5 run the online softmax (thread = query row = TMEM lane,
+// warp w on lanes 32*(w%4) ..) and the epilogue.  The MMA warp keeps the
+// tensor pipe one score tile ahead: S(j+1) is computed while the softmax
+// works on tile j, and S(j+2) is issued right after P(j) V.
+//
+// Online softmax in base 2 with lazy rescaling: the running maximum moves,
+// and the warp's rows of O are rescaled in TMEM, only when a tile's maximum
+// exceeds it by more than 8 (a factor of 256); otherwise the probabilities
+// are taken against the stale maximum, which leaves O / l exact.
+//
+// Every wait is bounded; a lost wait records MLA_ERR_TIMEOUT in the
+// workspace's error word and the CTA drains its copies and MMAs, frees TMEM
+// and returns.
+#include <math.h>
+
+#include "internal.cuh"
+#include "ptx.cuh"
+#include "tc.cuh"
+#include "tmap.cuh"
+
+namespace mla {
+namespace {
+
+constexpr int kQT = 128;  // queries per CTA
+constexpr int kKT = 128;  // keys per tile
+constexpr int kDh = 128, kDr = 64, kDc = 512;
+constexpr int kThreads = 192;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;  // log2(256)
+
+// ---- shared memory (offsets from the 1024-aligned dynamic base)
+constexpr uint32_t kBox = 128 * 128;  // 128 rows x 64 bf16 (128 B), 128B swizzle
+// query tile: boxes q_nope[0:64], q_nope[64:128], q_rope
+constexpr uint32_t kOffQ = 0;
+// K stage: boxes k_nope[0:64], k_nope[64:128], k_R (the same layout as Q)
+constexpr uint32_t kKStage = 3 * kBox;
+constexpr uint32_t kOffK = kOffQ + 3 * kBox;
+// V stage: boxes v[0:64], v[64:128]
+constexpr uint32_t kVStage = 2 * kBox;
+constexpr uint32_t kOffV = kOffK + 2 * kKStage;
+constexpr uint32_t kOffBars = kOffV + 2 * kVStage;
+
+struct Bars {
+  uint64_t q_full;
+  uint64_t k_full[2], k_empty[2];  // K ring
+  uint64_t v_full[2], v_empty[2];  // V ring
+  uint64_t s_full[2];              // scores of tile j in buffer j % 2
+  uint64_t p_full[2];              // probabilities of tile j written (one arrival per warp)
+  uint64_t pv_done[2];             // P(j) V accumulated (buffer j % 2 free again)
+  uint64_t o_done;
+  uint64_t drain;
+  uint32_t tmem;
+  int fail;
+};
+constexpr uint32_t kSmemBytes = 1024 + kOffBars + ((sizeof(Bars) + 15) / 16) * 16;
+static_assert(kSmemBytes <= 232448, "over the 227 KB shared-memory limit");
+
+// TMEM columns
+constexpr uint32_t kTmemS = 0;    // 2 x 128 fp32
+constexpr uint32_t kTmemO = 256;  // 128 fp32
+constexpr uint32_t kTmemP = 384;  // 2 x 64 (128 bf16 each, two per column)
+
+struct PrefillArgs {
+  const int32_t *cu_seqlens;  // [B + 1]
+  int B, H, max_seqlen, total;
+  float scale_log2;
+  __nv_bfloat16 *out;  // [total][H][128]
+  float *lse;          // [total][H]
+  int *err;
+};
+
+__device__ __forceinline__ bool wait_warp(uint64_t *bar, uint32_t parity, volatile int *fail) {
+  return __all_sync(0xffffffffu, ptx::mbar_wait(bar, parity, fail));
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_q,   // q_nope [total][H*128]
+                        const __grid_constant__ CUtensorMap tm_qr,  // q_rope [total][H*64]
+                        const __grid_constant__ CUtensorMap tm_kv,  // [K_nope | V] [total][H*256]
+                        const __grid_constant__ CUtensorMap tm_kr,  // k_R [total][64]
+                        PrefillArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Bars *bars = reinterpret_cast<Bars *>(smem + kOffBars);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.x, b = blockIdx.y;
+  const int qt = (int)gridDim.z - 1 - (int)blockIdx.z;  // heaviest tiles launch first
+
+  const int tok0 = a.cu_seqlens[b];
+  const int T = a.cu_seqlens[b + 1] - tok0;
+  if (tok0 < 0 || T < 0 || T > a.max_seqlen || tok0 > a.total - T) {
+    if (threadIdx.x == 0) set_device_error(a.err, kDevBounds);
+    return;
+  }
+  const int q0 = qt * kQT;
+  if (q0 >= T) return;
+  // key tiles 0 .. qt: the tile's first query sees key 128 qt, so every tile
+  // holds a visible key for every row
+  const int n = qt + 1;
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(&bars->q_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(&bars->k_full[i], 1);
+      ptx::mbar_init(&bars->k_empty[i], 1);
+      ptx::mbar_init(&bars->v_full[i], 1);
+      ptx::mbar_init(&bars->v_empty[i], 1);
+      ptx::mbar_init(&bars->s_full[i], 1);
+      ptx::mbar_init(&bars->p_full[i], 4);
+      ptx::mbar_init(&bars->pv_done[i], 1);
+    }
+    ptx::mbar_init(&bars->o_done, 1);
+    ptx::mbar_init(&bars->drain, 1);
+    bars->fail = 0;
+    ptx::fence_mbar_init();
+    ptx::tma_prefetch_desc(&tm_q);
+    ptx::tma_prefetch_desc(&tm_qr);
+    ptx::tma_prefetch_desc(&tm_kv);
+    ptx::tma_prefetch_desc(&tm_kr);
+  }
+  if (warp == 1) ptx::tmem_alloc(&bars->tmem, 512);
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = bars->tmem;
+  volatile int *fail = &bars->fail;
+
+  if (warp == 0) {
+    // ================= TMA producer =================
+    if (lane == 0) {
+      const int xq = h * kDh, xr = h * kDr, xk = h * 2 * kDh;
+      int nk = 0, nv = 0;
+      ptx::mbar_arrive_expect_tx(&bars->q_full, 3 * kBox);
+      ptx::tma_load_2d(smem + kOffQ, &tm_q, &bars->q_full, xq, tok0 + q0);
+      ptx::tma_load_2d(smem + kOffQ + kBox, &tm_q, &bars->q_full, xq + 64, tok0 + q0);
+      ptx::tma_load_2d(smem + kOffQ + 2 * kBox, &tm_qr, &bars->q_full, xr, tok0 + q0);
+      bool ok = true;
+      for (int j = 0; j < n; ++j) {
+        const int s = j & 1, y = tok0 + j * kKT;
+        if (j >= 2 && !ptx::mbar_wait(&bars->k_empty[s], ((j - 2) >> 1) & 1, fail)) {
+          ok = false;
+          break;
+        }
+        uint8_t *kd = smem + kOffK + s * kKStage;
+        ptx::mbar_arrive_expect_tx(&bars->k_full[s], kKStage);
+        ptx::tma_load_2d(kd, &tm_kv, &bars->k_full[s], xk, y);
+        ptx::tma_load_2d(kd + kBox, &tm_kv, &bars->k_full[s], xk + 64, y);
+        ptx::tma_load_2d(kd + 2 * kBox, &tm_kr, &bars->k_full[s], 0, y);
+        ++nk;
+        if (j >= 2 && !ptx::mbar_wait(&bars->v_empty[s], ((j - 2) >> 1) & 1, fail)) {
+          ok = false;
+          break;
+        }
+        uint8_t *vd = smem + kOffV + s * kVStage;
+        ptx::mbar_arrive_expect_tx(&bars->v_full[s], kVStage);
+        ptx::tma_load_2d(vd, &tm_kv, &bars->v_full[s], xk + kDh, y);
+        ptx::tma_load_2d(vd + kBox, &tm_kv, &bars->v_full[s], xk + kDh + 64, y);
+        ++nv;
+      }
+      if (!ok) atomicExch(const_cast<int *>(fail), 1);
+      // never leave with copies in flight: each ring's last fills have landed
+      ptx::mbar_wait(&bars->q_full, 0);
+      for (int j = nk - 2 < 0 ? 0 : nk - 2; j < nk; ++j)
+        ptx::mbar_wait(&bars->k_full[j & 1], (j >> 1) & 1);
+      for (int j = nv - 2 < 0 ? 0 : nv - 2; j < nv; ++j)
+        ptx::mbar_wait(&bars->v_full[j & 1], (j >> 1) & 1);
+    }
+  } else if (warp == 1) {
+    // ================= MMA issuer =================
+    if (lane == 0) {
+      const uint32_t idesc_s = ptx::idesc_bf16(kQT, kKT, false, false);
+      const uint32_t idesc_o = ptx::idesc_bf16(kQT, kDh, false, true);
+      const uint64_t qdesc = ptx::smem_desc(ptx::smem_u32(smem + kOffQ), 16, 1024, ptx::kSw128);
+      const uint64_t kdesc = ptx::smem_desc(ptx::smem_u32(smem + kOffK), 16, 1024, ptx::kSw128);
+      // V is MN-major: the two 64-wide d_v blocks are one box (kBox) apart
+      const uint64_t vdesc = ptx::smem_desc(ptx::smem_u32(smem + kOffV), kBox, 1024, ptx::kSw128);
+      auto issue_qk = [&](int j) -> bool {
+        const int s = j & 1;
+        if (!ptx::mbar_wait(&bars->k_full[s], (j >> 1) & 1, fail)) return false;
+        ptx::tc_fence_after();
+        const uint64_t kd = kdesc + (uint64_t)((s * kKStage) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < 12; ++kk) {  // 3 boxes x 4 k-steps of 16
+          const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
+          ptx::mma_bf16(tmem + kTmemS + s * kKT, qdesc + (uint64_t)(off >> 4),
+                        kd + (uint64_t)(off >> 4), idesc_s, kk != 0);
+        }
+        ptx::mma_commit(&bars->s_full[s]);
+        ptx::mma_commit(&bars->k_empty[s]);
+        return true;
+      };
+      bool ok = ptx::mbar_wait(&bars->q_full, 0, fail);
+      ptx::tc_fence_after();
+      if (ok) ok = issue_qk(0);
+      if (ok && n > 1) ok = issue_qk(1);
+      for (int j = 0; j < n && ok; ++j) {
+        const int s = j & 1;
+        if (!ptx::mbar_wait(&bars->p_full[s], (j >> 1) & 1, fail) ||
+            !ptx::mbar_wait(&bars->v_full[s], (j >> 1) & 1, fail)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint64_t vd = vdesc + (uint64_t)((s * kVStage) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < kKT / 16; ++kk)
+          ptx::mma_bf16_ts(tmem + kTmemO, tmem + kTmemP + s * 64 + kk * 8,
+                           vd + (uint64_t)((kk * 2048) >> 4), idesc_o, (j | kk) != 0);
+        ptx::mma_commit(&bars->pv_done[s]);
+        ptx::mma_commit(&bars->v_empty[s]);
+        if (j + 2 < n) ok = issue_qk(j + 2);
+      }
+      if (ok) ptx::mma_commit(&bars->o_done);
+      else atomicExch(const_cast<int *>(fail), 1);
+      // every MMA issued above has completed before TMEM is freed
+      ptx::mma_commit(&bars->drain);
+      ptx::mbar_wait(&bars->drain, 0);
+    }
+  } else {
+    // ================= softmax and epilogue (warps 2-5) =================
+    const int wq = warp & 3;
+    const int row = wq * 32 + lane;  // query row of the tile = TMEM lane
+    const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+    const int q = q0 + row;                 // position in the sequence
+    const int qlim = q < T ? q : T - 1;     // last visible key (rows past T: all keys)
+    float m_used = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n; ++j) {
+      const int s = j & 1;
+      if (!wait_warp(&bars->s_full[s], (j >> 1) & 1, fail)) {
+        ok = false;
+        break;
+      }
+      ptx::tc_fence_after();
+      float x[kKT];
+#pragma unroll
+      for (int c = 0; c < kKT; c += 16) {
+        float v[16];
+        ptx::tmem_ld16(tmem + lane_base + kTmemS + s * kKT + c, v);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) x[c + i] = v[i];
+      }
+      ptx::tmem_ld_wait();
+      // base-2 logits; keys past this row's position are masked
+      const int lim = qlim - j * kKT;
+      float mt = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < kKT; ++c) {
+        x[c] = c <= lim ? x[c] * a.scale_log2 : -INFINITY;
+        mt = fmaxf(mt, x[c]);
+      }
+      const bool grow = mt > m_used + kRescaleThreshold;
+      float alpha = 1.f;
+      if (grow) {
+        alpha = ptx::ex2(m_used - mt);  // 0 on the first tile (m_used = -inf)
+        m_used = mt;
+      }
+      l *= alpha;
+      if (j > 0 && __any_sync(0xffffffffu, grow)) {
+        // O holds tiles 0 .. j-1: rescale this warp's rows once P(j-1) V is in
+        if (!wait_warp(&bars->pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, fail)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < kDh; c += 16) {
+          float v[16];
+          ptx::tmem_ld16(tmem + lane_base + kTmemO + c, v);
+          ptx::tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v[i] *= alpha;
+          ptx::tmem_st16(tmem + lane_base + kTmemO + c, v);
+        }
+      }
+      // P buffer s was last read by P(j-2) V
+      if (j >= 2 && !wait_warp(&bars->pv_done[s], ((j - 2) >> 1) & 1, fail)) {
+        ok = false;
+        break;
+      }
+      ptx::tc_fence_after();
+      float ls = 0.f;
+#pragma unroll
+      for (int c = 0; c < kKT; c += 32) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float p0 = ptx::ex2(x[c + 2 * i] - m_used);
+          const float p1 = ptx::ex2(x[c + 2 * i + 1] - m_used);
+          ls += p0 + p1;
+          pk[i] = ptx::pack_bf16x2(p0, p1);
+        }
+        ptx::tmem_st16_nc(tmem + lane_base + kTmemP + s * 64 + c / 2, pk);
+      }
+      l += ls;
+      ptx::tmem_st_wait();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&bars->p_full[s]);
+    }
+    if (ok && !wait_warp(&bars->o_done, 0, fail)) ok = false;
+    if (ok) {
+      ptx::tc_fence_after();
+      const bool store = q < T;
+      const float inv = 1.f / l;
+      const size_t orow = (size_t)(tok0 + (store ? q : 0)) * a.H + h;
+#pragma unroll
+      for (int c = 0; c < kDh; c += 16) {
+        float v[16];
+        ptx::tmem_ld16(tmem + lane_base + kTmemO + c, v);
+        ptx::tmem_ld_wait();
+        uint32_t pk[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) pk[i] = ptx::pack_bf16x2(v[2 * i] * inv, v[2 * i + 1] * inv);
+        if (store) {
+          uint4 *d4 = reinterpret_cast<uint4 *>(a.out + orow * kDh + c);
+          d4[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          d4[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        }
+      }
+      if (store) a.lse[orow] = (m_used + log2f(l)) * kLn2;
+    } else {
+      atomicExch(const_cast<int *>(fail), 1);
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 512);
+  }
+  if (threadIdx.x == 0 && bars->fail) set_device_error(a.err, kDevTimeout);
+}
+
+}  // namespace
+
+bool tc_prefill_supported(const mla_dims &d) {
+  return d.dtype == MLA_BF16 && d.d_h == kDh && d.d_c == kDc && d.d_r == kDr;
+}
+
+size_t prefill_workspace_bytes(int total, const mla_dims &d) {
+  return kWsHeader + align_up((size_t)total * d.H * 2 * kDh * sizeof(__nv_bfloat16), 256);
+}
+
+cudaError_t launch_prefill_tc(const void *q_nope, const void *q_rope, const void *c_kv,
+                              const void *k_r, const void *W_UK, const void *W_UV,
+                              const int32_t *cu_seqlens, int B, int max_seqlen, int total,
+                              const mla_dims &d, float scale, void *out, float *lse,
+                              void *workspace, cudaStream_t st) {
+  char *ws = static_cast<char *>(workspace);
+  void *kv = ws + kWsHeader;
+  // [K_nope | V] of every (token, head): [total][H][256]
+  cudaError_t e = launch_kv_up_tc(c_kv, W_UK, W_UV, kv, total, d, st);
+  if (e != cudaSuccess) return e;
+  const uint64_t H = (uint64_t)d.H;
+  CUtensorMap tm_q, tm_qr, tm_kv, tm_kr;
+  if (!make_tmap_2d_bf16(&tm_q, q_nope, H * kDh, total, H * kDh * 2, 64, kQT,
+                         CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap_2d_bf16(&tm_qr, q_rope, H * kDr, total, H * kDr * 2, 64, kQT,
+                         CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap_2d_bf16(&tm_kv, kv, H * 2 * kDh, total, H * 2 * kDh * 2, 64, kKT,
+                         CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap_2d_bf16(&tm_kr, k_r, kDr, total, kDr * 2, 64, kKT, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  e = cudaFuncSetAttribute(prefill_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)kSmemBytes);
+  if (e != cudaSuccess) return e;
+  PrefillArgs a;
+  a.cu_seqlens = cu_seqlens;
+  a.B = B;
+  a.H = d.H;
+  a.max_seqlen = max_seqlen;
+  a.total = total;
+  a.scale_log2 = scale * kLog2e;
+  a.out = static_cast<__nv_bfloat16 *>(out);
+  a.lse = lse;
+  a.err = reinterpret_cast<int *>(ws);
+  const dim3 grid(d.H, B, (max_seqlen + kQT - 1) / kQT);
+  prefill_attn_kernel<<<grid, kThreads, kSmemBytes, st>>>(tm_q, tm_qr, tm_kv, tm_kr, a);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

@@ -171,6 +171,39 @@ def test_project_query_host_validation():
     assert lib.mla_project_query(*empty) == m.MLA_OK
 
 
+def test_prefill_host_validation():
+    lib = m.raw_lib()
+    d = ctypes.byref(_dims())
+    n = ctypes.c_size_t()
+    assert lib.mla_prefill_workspace_size(4096, d, ctypes.byref(n)) == m.MLA_OK
+    # error-word header plus [K_nope | V] in bf16 per (token, head)
+    assert n.value == 256 + 4096 * 128 * 256 * 2
+    assert lib.mla_prefill_workspace_size(-1, d, ctypes.byref(n)) == m.MLA_ERR_INVALID_ARG
+    bad_dims = ctypes.byref(m.Dims(128, 128, 512, 32))
+    assert lib.mla_prefill_workspace_size(16, bad_dims, ctypes.byref(n)) == m.MLA_ERR_UNSUPPORTED
+    ok = ctypes.c_void_p(1 << 20)
+    mis = ctypes.c_void_p((1 << 20) + 8)
+    args = [ok, ok, ok, ok, ok, ok, ok, 2, 300, 500, d, ok, ok, ok, 1 << 30, None]
+    for i in (0, 1, 2, 3, 4, 5, 11):  # tensors must be 16-byte aligned
+        bad = list(args); bad[i] = mis
+        assert lib.mla_prefill(*bad) == m.MLA_ERR_INVALID_ARG, i
+    bad = list(args); bad[6] = None
+    assert lib.mla_prefill(*bad) == m.MLA_ERR_INVALID_ARG
+    bad = list(args); bad[14] = 1 << 20
+    assert lib.mla_prefill(*bad) == m.MLA_ERR_WORKSPACE
+    bad = list(args); bad[13] = mis
+    assert lib.mla_prefill(*bad) == m.MLA_ERR_WORKSPACE
+    bad = list(args); bad[7] = 70000
+    assert lib.mla_prefill(*bad) == m.MLA_ERR_INVALID_ARG
+    bad = list(args); bad[10] = bad_dims
+    assert lib.mla_prefill(*bad) == m.MLA_ERR_UNSUPPORTED
+    for i in (7, 9):  # no sequences or no tokens: nothing to do
+        empty = list(args); empty[i] = 0
+        assert lib.mla_prefill(*empty) == m.MLA_OK
+    bad = list(args); bad[8] = 0  # tokens, but no sequence may hold one
+    assert lib.mla_prefill(*bad) == m.MLA_ERR_INVALID_ARG
+
+
 def test_empty_batch_is_a_noop():
     lib = m.raw_lib()
     d = ctypes.byref(_dims())
