@@ -284,39 +284,6 @@ cudaError_t launch_out_proj_tc(const void *o_lat, const void *W_UV, void *out, i
   return launch_head_gemm<false>(tmA, tmA, tmB, g, 1, st);
 }
 
-// ---- prefill: keys and values rebuilt from the latents ----
-//
-// ("MLA, dim by dim" 4.1: K = C^KV W_UK, V = C^KV W_UV before the quadratic
-// contractions.)  kv[t, h, 0:128] = W_UK[h] c_t and kv[t, h, 128:256] =
-// W_UV[h] c_t: D[m][t] = A[m][c] B[t][c] with M = 2 x 128 (M tile 0 reads
-// W_UK, tile 1 W_UV), N = tokens, K = d_c; every head reads the same latents.
-cudaError_t launch_kv_up_tc(const void *c_kv, const void *W_UK, const void *W_UV, void *kv,
-                            int T, const mla_dims &d, cudaStream_t st) {
-  CUtensorMap tmA, tmA2, tmB;
-  const int Nt = pick_nt(T);
-  if (!make_tmap_2d_bf16(&tmA, W_UK, d.d_c, (uint64_t)d.H * d.d_h, (uint64_t)d.d_c * 2, 64, 128,
-                         CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_tmap_2d_bf16(&tmA2, W_UV, d.d_c, (uint64_t)d.H * d.d_h, (uint64_t)d.d_c * 2, 64,
-                         128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_tmap_2d_bf16(&tmB, c_kv, d.d_c, T, (uint64_t)d.d_c * 2, 64, Nt,
-                         CU_TENSOR_MAP_SWIZZLE_128B))
-    return cudaErrorInvalidValue;
-  GemmArgs g;
-  g.num_k_chunks = d.d_c / kKChunk;
-  g.rows = T;
-  g.Nt = Nt;
-  g.H = d.H;
-  g.M_total = 2 * d.d_h;
-  g.a_rows_per_head = d.d_h;
-  g.a_cols_per_head = 0;
-  g.b_cols_per_head = 0;
-  g.out = static_cast<__nv_bfloat16 *>(kv);
-  g.part = nullptr;
-  g.m_ofs = 0;
-  g.a_tiles = 1;
-  return launch_head_gemm<false>(tmA, tmA2, tmB, g, 2, st);
-}
-
 // ---- fused latent / RoPE-key projection into the paged cache ----
 
 namespace {

@@ -8,11 +8,13 @@
 //   S = [q_nope ; q_rope] K^T * scale,   causal row softmax,   out = P V
 // with lse the natural log-sum-exp of the scaled scores.  Absorbing W_UK and
 // W_UV here would move the T^2 contractions from 192 / 128 onto d_c = 512,
-// so unlike decode the up-projections run first: one tensor-core GEMM writes
-// [K_nope | V] per (token, head) into the workspace (head_gemm_kernel), and
-// this kernel reads it.
+// so unlike decode the up-projections run first: kv_rebuild_kernel writes
+// [K_nope | V] per (token, head) into the workspace, and prefill_attn_kernel
+// reads it.
 //
-// One CTA per (head, sequence, 128-query tile), heaviest query tiles first.
+// One CTA per (128-query tile, head, sequence); the query tiles of one head
+// are adjacent in the grid (heaviest first), so their shared K and V tiles
+// stay in L2 instead of being read from HBM once per query tile.
 // Queries are the MMA M dimension (128 rows = TMEM lanes), keys come in
 // tiles of 128:
 //   S  = Q K^T    M=128, N=128, K=192  A = Q (smem), B = K tile (smem)
@@ -111,8 +113,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Bars *bars = reinterpret_cast<Bars *>(smem + kOffBars);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int h = blockIdx.x, b = blockIdx.y;
-  const int qt = (int)gridDim.z - 1 - (int)blockIdx.z;  // heaviest tiles launch first
+  // query tiles vary fastest, so the CTAs that share one head's K and V run
+  // together and read them from L2; heaviest tiles first within each head
+  const int qt = (int)gridDim.x - 1 - (int)blockIdx.x;
+  const int h = blockIdx.y, b = blockIdx.z;
 
   const int tok0 = a.cu_seqlens[b];
   const int T = a.cu_seqlens[b + 1] - tok0;
@@ -361,6 +365,215 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0 && bars->fail) set_device_error(a.err, kDevTimeout);
 }
 
+// ---- keys and values rebuilt from the latents ----
+//
+// kv[t, h, 0:128] = W_UK[h] c_t and kv[t, h, 128:256] = W_UV[h] c_t for a
+// tile of 128 tokens and kRebuildHeads consecutive heads per CTA:
+//   D[t][n] = sum_c C[t][c] W[n][c]   M = 128 tokens, N = 256 (W_UK[h] rows
+//   then W_UV[h] rows), K = d_c = 512
+// The latent tile (128 x 512, 128 KB) is loaded once and stays in shared
+// memory; the weights stream through a ring of 64-wide K chunks (W_UK and
+// W_UV boxes side by side: one 256-row K-major operand).  Two TMEM
+// accumulators (256 columns each) let the epilogue of one head overlap the
+// MMAs of the next.  Thread = token row = TMEM lane, so each thread writes
+// its token's 512 contiguous bytes of the head.
+constexpr int kRebuildHeads = 8;
+constexpr int kRStages = 3;
+constexpr uint32_t kRBoxA = 128 * 128;       // 128 tokens x 64 latents
+constexpr uint32_t kROffA = 0;                // 8 boxes: latents 0-63, 64-127, ...
+constexpr uint32_t kROffB = 8 * kRBoxA;       // ring of [W_UK chunk ; W_UV chunk]
+constexpr uint32_t kRStage = 2 * 128 * 128;   // 256 rows x 128 B
+constexpr uint32_t kROffBars = kROffB + kRStages * kRStage;
+
+struct RBars {
+  uint64_t a_full;
+  uint64_t b_full[kRStages], b_empty[kRStages];
+  uint64_t acc_full[2], acc_empty[2];
+  uint64_t drain;
+  uint32_t tmem;
+  int fail;
+};
+constexpr uint32_t kRSmemBytes = 1024 + kROffBars + ((sizeof(RBars) + 15) / 16) * 16;
+static_assert(kRSmemBytes <= 232448, "over the 227 KB shared-memory limit");
+
+struct RebuildArgs {
+  int T, H;
+  __nv_bfloat16 *kv;  // [T][H][256]
+  int *err;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    kv_rebuild_kernel(const __grid_constant__ CUtensorMap tm_c,    // c_kv [T][512]
+                      const __grid_constant__ CUtensorMap tm_wuk,  // W_UK [H*128][512]
+                      const __grid_constant__ CUtensorMap tm_wuv,  // W_UV [H*128][512]
+                      RebuildArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  RBars *bars = reinterpret_cast<RBars *>(smem + kROffBars);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t0 = blockIdx.x * 128;
+  const int h0 = blockIdx.y * kRebuildHeads;
+  const int nh = a.H - h0 < kRebuildHeads ? a.H - h0 : kRebuildHeads;
+  constexpr int kChunks = kDc / 64;
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(&bars->a_full, 1);
+    for (int i = 0; i < kRStages; ++i) {
+      ptx::mbar_init(&bars->b_full[i], 1);
+      ptx::mbar_init(&bars->b_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(&bars->acc_full[i], 1);
+      ptx::mbar_init(&bars->acc_empty[i], 4);
+    }
+    ptx::mbar_init(&bars->drain, 1);
+    bars->fail = 0;
+    ptx::fence_mbar_init();
+    ptx::tma_prefetch_desc(&tm_c);
+    ptx::tma_prefetch_desc(&tm_wuk);
+    ptx::tma_prefetch_desc(&tm_wuv);
+  }
+  if (warp == 1) ptx::tmem_alloc(&bars->tmem, 512);
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = bars->tmem;
+  volatile int *fail = &bars->fail;
+
+  if (warp == 0) {
+    // ================= TMA producer =================
+    if (lane == 0) {
+      ptx::mbar_arrive_expect_tx(&bars->a_full, 8 * kRBoxA);
+      for (int k = 0; k < kChunks; ++k)
+        ptx::tma_load_2d(smem + kROffA + k * kRBoxA, &tm_c, &bars->a_full, k * 64, t0);
+      const int nf = nh * kChunks;
+      int f = 0;
+      for (; f < nf; ++f) {
+        const int s = f % kRStages, h = h0 + f / kChunks, k = f % kChunks;
+        if (f >= kRStages &&
+            !ptx::mbar_wait(&bars->b_empty[s], ((f / kRStages) - 1) & 1, fail)) {
+          atomicExch(const_cast<int *>(fail), 1);
+          break;
+        }
+        uint8_t *dst = smem + kROffB + s * kRStage;
+        ptx::mbar_arrive_expect_tx(&bars->b_full[s], kRStage);
+        ptx::tma_load_2d(dst, &tm_wuk, &bars->b_full[s], k * 64, h * kDh);
+        ptx::tma_load_2d(dst + kRStage / 2, &tm_wuv, &bars->b_full[s], k * 64, h * kDh);
+      }
+      // never leave with copies in flight
+      ptx::mbar_wait(&bars->a_full, 0);
+      for (int i = f - kRStages < 0 ? 0 : f - kRStages; i < f; ++i)
+        ptx::mbar_wait(&bars->b_full[i % kRStages], (i / kRStages) & 1);
+    }
+  } else if (warp == 1) {
+    // ================= MMA issuer =================
+    if (lane == 0) {
+      const uint32_t idesc = ptx::idesc_bf16(128, 256, false, false);
+      const uint64_t adesc = ptx::smem_desc(ptx::smem_u32(smem + kROffA), 16, 1024, ptx::kSw128);
+      const uint64_t bdesc = ptx::smem_desc(ptx::smem_u32(smem + kROffB), 16, 1024, ptx::kSw128);
+      bool ok = ptx::mbar_wait(&bars->a_full, 0, fail);
+      ptx::tc_fence_after();
+      for (int g = 0; g < nh && ok; ++g) {
+        const int buf = g & 1;
+        if (g >= 2 && !ptx::mbar_wait(&bars->acc_empty[buf], ((g - 2) >> 1) & 1, fail)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        for (int k = 0; k < kChunks; ++k) {
+          const int f = g * kChunks + k, s = f % kRStages;
+          if (!ptx::mbar_wait(&bars->b_full[s], (f / kRStages) & 1, fail)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint64_t ad = adesc + (uint64_t)((k * kRBoxA) >> 4);
+          const uint64_t bd = bdesc + (uint64_t)((s * kRStage) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            ptx::mma_bf16(tmem + buf * 256, ad + (uint64_t)((kk * 32) >> 4),
+                          bd + (uint64_t)((kk * 32) >> 4), idesc, (k | kk) != 0);
+          ptx::mma_commit(&bars->b_empty[s]);
+        }
+        if (ok) ptx::mma_commit(&bars->acc_full[buf]);
+      }
+      if (!ok) atomicExch(const_cast<int *>(fail), 1);
+      ptx::mma_commit(&bars->drain);
+      ptx::mbar_wait(&bars->drain, 0);
+    }
+  } else {
+    // ================= epilogue (warps 2-5) =================
+    const int wq = warp & 3;
+    const int row = wq * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+    const bool store = t0 + row < a.T;
+    for (int g = 0; g < nh; ++g) {
+      const int buf = g & 1;
+      if (!wait_warp(&bars->acc_full[buf], (g >> 1) & 1, fail)) {
+        atomicExch(const_cast<int *>(fail), 1);
+        break;
+      }
+      ptx::tc_fence_after();
+      __nv_bfloat16 *dst = a.kv + ((size_t)(store ? t0 + row : 0) * a.H + h0 + g) * 256;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        float v[8][16];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          ptx::tmem_ld16(tmem + lane_base + buf * 256 + half * 128 + i * 16, v[i]);
+        ptx::tmem_ld_wait();
+        if (store) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            uint32_t pk[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) pk[e] = ptx::pack_bf16x2(v[i][2 * e], v[i][2 * e + 1]);
+            uint4 *d4 = reinterpret_cast<uint4 *>(dst + half * 128 + i * 16);
+            d4[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            d4[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&bars->acc_empty[buf]);
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 512);
+  }
+  if (threadIdx.x == 0 && bars->fail) set_device_error(a.err, kDevTimeout);
+}
+
+cudaError_t launch_kv_rebuild(const void *c_kv, const void *W_UK, const void *W_UV, void *kv,
+                              int T, const mla_dims &d, int *err, cudaStream_t st) {
+  const uint64_t rows = (uint64_t)d.H * kDh;
+  CUtensorMap tm_c, tm_wuk, tm_wuv;
+  if (!make_tmap_2d_bf16(&tm_c, c_kv, kDc, T, kDc * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap_2d_bf16(&tm_wuk, W_UK, kDc, rows, kDc * 2, 64, 128,
+                         CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap_2d_bf16(&tm_wuv, W_UV, kDc, rows, kDc * 2, 64, 128,
+                         CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(kv_rebuild_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)kRSmemBytes);
+  if (e != cudaSuccess) return e;
+  RebuildArgs a;
+  a.T = T;
+  a.H = d.H;
+  a.kv = static_cast<__nv_bfloat16 *>(kv);
+  a.err = err;
+  const dim3 grid((T + 127) / 128, (d.H + kRebuildHeads - 1) / kRebuildHeads);
+  kv_rebuild_kernel<<<grid, kThreads, kRSmemBytes, st>>>(tm_c, tm_wuk, tm_wuv, a);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 bool tc_prefill_supported(const mla_dims &d) {
@@ -379,7 +592,8 @@ cudaError_t launch_prefill_tc(const void *q_nope, const void *q_rope, const void
   char *ws = static_cast<char *>(workspace);
   void *kv = ws + kWsHeader;
   // [K_nope | V] of every (token, head): [total][H][256]
-  cudaError_t e = launch_kv_up_tc(c_kv, W_UK, W_UV, kv, total, d, st);
+  cudaError_t e = launch_kv_rebuild(c_kv, W_UK, W_UV, kv, total, d, reinterpret_cast<int *>(ws),
+                                    st);
   if (e != cudaSuccess) return e;
   const uint64_t H = (uint64_t)d.H;
   CUtensorMap tm_q, tm_qr, tm_kv, tm_kr;
@@ -404,7 +618,7 @@ cudaError_t launch_prefill_tc(const void *q_nope, const void *q_rope, const void
   a.out = static_cast<__nv_bfloat16 *>(out);
   a.lse = lse;
   a.err = reinterpret_cast<int *>(ws);
-  const dim3 grid(d.H, B, (max_seqlen + kQT - 1) / kQT);
+  const dim3 grid((max_seqlen + kQT - 1) / kQT, d.H, B);
   prefill_attn_kernel<<<grid, kThreads, kSmemBytes, st>>>(tm_q, tm_qr, tm_kv, tm_kr, a);
   return cudaGetLastError();
 }

@@ -48,12 +48,10 @@ cudaError_t launch_qproj_tc(const void *h, const void *W_Q, const void *W_QR, in
                             cudaStream_t st);
 
 // bf16, d_h = 128, d_c = 512, d_r = 64 (prefill in the standard order:
-// [K_nope | V] per token and head by a tensor-core GEMM into the workspace,
+// [K_nope | V] per token and head rebuilt on tcgen05 into the workspace,
 // then causal attention on tcgen05).
 bool tc_prefill_supported(const mla_dims &d);
 size_t prefill_workspace_bytes(int total, const mla_dims &d);
-cudaError_t launch_kv_up_tc(const void *c_kv, const void *W_UK, const void *W_UV, void *kv,
-                            int T, const mla_dims &d, cudaStream_t st);
 cudaError_t launch_prefill_tc(const void *q_nope, const void *q_rope, const void *c_kv,
                               const void *k_r, const void *W_UK, const void *W_UV,
                               const int32_t *cu_seqlens, int B, int max_seqlen, int total,
