@@ -17,19 +17,25 @@
 // stay in L2 instead of being read from HBM once per query tile.
 // Queries are the MMA M dimension (128 rows = TMEM lanes), keys come in
 // tiles of 128:
-//   S  = Q K^T    M=128, N=128, K=192  A = Q (smem), B = K tile (smem)
+//   S  = Q K^T    M=128, N=128, K=192  A = Q (TMEM), B = K tile (smem)
 //   O += P V      M=128, N=128, K=128  A = P (TMEM, bf16), B = V tile (smem,
 //                                       MN-major)
-// TMEM (512 columns): two 128-column score buffers, the 128-column output
-// accumulator, two 64-column buffers of packed bf16 probabilities.  Shared
-// memory: the query tile (48 KB) and two stages each of K (48 KB) and V
-// (32 KB) tiles, all 128-byte swizzled, loaded by TMA.
+// TMEM (512 columns): the 128-column score tile, the 128-column output
+// accumulator, two 64-column buffers of packed bf16 probabilities and the
+// query (96 columns).  Shared memory: a ring of three K stages (48 KB: the
+// two halves of K_nope and k_R) whose first fill is the query tile on its
+// way into TMEM, and a ring of two V stages (32 KB), all 128-byte swizzled
+// and loaded by TMA.  Keeping the query out of shared memory buys the third
+// K stage, which hides the L2 latency of the next key tile.
 //
-// Warp roles (192 threads): warp 0 issues TMA, warp 1 owns TMEM and issues
-// MMAs, warps 2-5 run the online softmax (thread = query row = TMEM lane,
-// warp w on lanes 32*(w%4) ..) and the epilogue.  The MMA warp keeps the
-// tensor pipe one score tile ahead: S(j+1) is computed while the softmax
-// works on tile j, and S(j+2) is issued right after P(j) V.
+// Warp roles (384 threads): warps 0 and 10 issue TMA (the query and the K
+// tiles; the V tiles), warp 1 owns TMEM and issues Q K^T, warp 11 issues
+// P V, warps 2-9 run the online softmax and the epilogue: thread = query row = TMEM lane, warps w
+// and w+4 on lanes 32*(w%4).. (one SM sub-partition), each taking half of a
+// tile's 128 key columns; the pair agrees on the row maximum through shared
+// memory and an mbarrier.  As soon as the softmax has read a score tile the
+// next Q K^T goes into the same columns, so the next scores are ready when
+// the softmax finishes; the P V of each tile follows its softmax.
 //
 // Online softmax in base 2 with lazy rescaling: the running maximum moves,
 // and the warp's rows of O are rescaled in TMEM, only when a tile's maximum
@@ -52,32 +58,42 @@ namespace {
 constexpr int kQT = 128;  // queries per CTA
 constexpr int kKT = 128;  // keys per tile
 constexpr int kDh = 128, kDr = 64, kDc = 512;
-constexpr int kThreads = 192;
+constexpr int kThreads = 384;   // attention: two TMA warps, two MMA warps, eight softmax warps
+constexpr int kRThreads = 192;  // rebuild: TMA, MMA, four epilogue warps
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2(256)
 
 // ---- shared memory (offsets from the 1024-aligned dynamic base)
 constexpr uint32_t kBox = 128 * 128;  // 128 rows x 64 bf16 (128 B), 128B swizzle
-// query tile: boxes q_nope[0:64], q_nope[64:128], q_rope
-constexpr uint32_t kOffQ = 0;
-// K stage: boxes k_nope[0:64], k_nope[64:128], k_R (the same layout as Q)
+// K ring: stage = boxes k_nope[0:64], k_nope[64:128], k_R.  The query tile
+// (boxes q_nope[0:64], q_nope[64:128], q_rope) is the ring's first fill, on
+// its way into TMEM.
+constexpr int kKStages = 3;
 constexpr uint32_t kKStage = 3 * kBox;
-constexpr uint32_t kOffK = kOffQ + 3 * kBox;
-// V stage: boxes v[0:64], v[64:128]
+constexpr uint32_t kOffK = 0;
+// V ring: stage = boxes v[0:64], v[64:128]
+constexpr int kVStages = 2;
 constexpr uint32_t kVStage = 2 * kBox;
-constexpr uint32_t kOffV = kOffK + 2 * kKStage;
-constexpr uint32_t kOffBars = kOffV + 2 * kVStage;
+constexpr uint32_t kOffV = kOffK + kKStages * kKStage;
+// softmax pair exchange: row maxima [tile parity][column half][128], row
+// sums [column half][128]
+constexpr uint32_t kOffRed = kOffV + kVStages * kVStage;
+constexpr uint32_t kOffBars = kOffRed + 6 * 128 * 4;
 
 struct Bars {
-  uint64_t q_full;
-  uint64_t k_full[2], k_empty[2];  // K ring
-  uint64_t v_full[2], v_empty[2];  // V ring
-  uint64_t s_full[2];              // scores of tile j in buffer j % 2
-  uint64_t p_full[2];              // probabilities of tile j written (one arrival per warp)
-  uint64_t pv_done[2];             // P(j) V accumulated (buffer j % 2 free again)
+  uint64_t k_full[kKStages], k_empty[kKStages];  // K ring (fill 0: the query)
+  uint64_t v_full[kVStages], v_empty[kVStages];  // V ring
+  uint64_t q_tmem;      // the query copied into TMEM (one arrival per softmax warp)
+  uint64_t s_full;      // scores of the current tile ready
+  uint64_t s_free;      // ... and read (one arrival per softmax warp)
+  uint64_t p_full[2];   // probabilities of tile j in buffer j % 2 (one arrival per warp)
+  uint64_t pv_done[2];  // P(j) V accumulated (buffer j % 2 free again)
   uint64_t o_done;
-  uint64_t drain;
+  uint64_t drain[2];  // each MMA issuer's last MMAs done
+  // softmax pairs: row maxima of tile j exchanged (per row quarter and tile
+  // parity), row sums exchanged at the end; 64 arrivals each
+  uint64_t pair_max[4][2], pair_sum[4];
   uint32_t tmem;
   int fail;
 };
@@ -85,10 +101,10 @@ constexpr uint32_t kSmemBytes = 1024 + kOffBars + ((sizeof(Bars) + 15) / 16) * 1
 static_assert(kSmemBytes <= 232448, "over the 227 KB shared-memory limit");
 
 // TMEM columns
-constexpr uint32_t kTmemS = 0;    // 2 x 128 fp32
-constexpr uint32_t kTmemO = 256;  // 128 fp32
-constexpr uint32_t kTmemP = 384;  // 2 x 64 (128 bf16 each, two per column)
-
+constexpr uint32_t kTmemS = 0;    // 128 fp32 scores
+constexpr uint32_t kTmemO = 128;  // 128 fp32 output accumulator
+constexpr uint32_t kTmemP = 256;  // 2 x 64 (128 bf16 probabilities each, two per column)
+constexpr uint32_t kTmemQ = 384;  // 96 (the 192 bf16 query elements of a row)
 struct PrefillArgs {
   const int32_t *cu_seqlens;  // [B + 1]
   int B, H, max_seqlen, total;
@@ -131,18 +147,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n = qt + 1;
 
   if (threadIdx.x == 0) {
-    ptx::mbar_init(&bars->q_full, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kKStages; ++i) {
       ptx::mbar_init(&bars->k_full[i], 1);
       ptx::mbar_init(&bars->k_empty[i], 1);
+    }
+    for (int i = 0; i < kVStages; ++i) {
       ptx::mbar_init(&bars->v_full[i], 1);
       ptx::mbar_init(&bars->v_empty[i], 1);
-      ptx::mbar_init(&bars->s_full[i], 1);
-      ptx::mbar_init(&bars->p_full[i], 4);
+    }
+    ptx::mbar_init(&bars->q_tmem, 8);
+    ptx::mbar_init(&bars->s_full, 1);
+    ptx::mbar_init(&bars->s_free, 8);
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(&bars->p_full[i], 8);
       ptx::mbar_init(&bars->pv_done[i], 1);
     }
     ptx::mbar_init(&bars->o_done, 1);
-    ptx::mbar_init(&bars->drain, 1);
+    ptx::mbar_init(&bars->drain[0], 1);
+    ptx::mbar_init(&bars->drain[1], 1);
+    for (int i = 0; i < 4; ++i) {
+      ptx::mbar_init(&bars->pair_max[i][0], 64);
+      ptx::mbar_init(&bars->pair_max[i][1], 64);
+      ptx::mbar_init(&bars->pair_sum[i], 64);
+    }
     bars->fail = 0;
     ptx::fence_mbar_init();
     ptx::tma_prefetch_desc(&tm_q);
@@ -156,131 +183,210 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = bars->tmem;
   volatile int *fail = &bars->fail;
+  const int xk = h * 2 * kDh;  // column of this head's [K_nope | V] in the workspace
 
   if (warp == 0) {
-    // ================= TMA producer =================
+    // ================= TMA producer: the query, then the K tiles =================
     if (lane == 0) {
-      const int xq = h * kDh, xr = h * kDr, xk = h * 2 * kDh;
-      int nk = 0, nv = 0;
-      ptx::mbar_arrive_expect_tx(&bars->q_full, 3 * kBox);
-      ptx::tma_load_2d(smem + kOffQ, &tm_q, &bars->q_full, xq, tok0 + q0);
-      ptx::tma_load_2d(smem + kOffQ + kBox, &tm_q, &bars->q_full, xq + 64, tok0 + q0);
-      ptx::tma_load_2d(smem + kOffQ + 2 * kBox, &tm_qr, &bars->q_full, xr, tok0 + q0);
+      ptx::mbar_arrive_expect_tx(&bars->k_full[0], kKStage);
+      ptx::tma_load_2d(smem + kOffK, &tm_q, &bars->k_full[0], h * kDh, tok0 + q0);
+      ptx::tma_load_2d(smem + kOffK + kBox, &tm_q, &bars->k_full[0], h * kDh + 64, tok0 + q0);
+      ptx::tma_load_2d(smem + kOffK + 2 * kBox, &tm_qr, &bars->k_full[0], h * kDr, tok0 + q0);
+      int f = 1;  // fill f of the ring is key tile f - 1
+      for (; f <= n; ++f) {
+        const int st = f % kKStages, y = tok0 + (f - 1) * kKT;
+        if (f >= kKStages &&
+            !ptx::mbar_wait(&bars->k_empty[st], ((f / kKStages) - 1) & 1, fail)) {
+          atomicExch(const_cast<int *>(fail), 1);
+          break;
+        }
+        uint8_t *kd = smem + kOffK + st * kKStage;
+        ptx::mbar_arrive_expect_tx(&bars->k_full[st], kKStage);
+        ptx::tma_load_2d(kd, &tm_kv, &bars->k_full[st], xk, y);
+        ptx::tma_load_2d(kd + kBox, &tm_kv, &bars->k_full[st], xk + 64, y);
+        ptx::tma_load_2d(kd + 2 * kBox, &tm_kr, &bars->k_full[st], 0, y);
+      }
+      // never leave with copies in flight: the ring's last fills have landed
+      for (int i = f - kKStages < 0 ? 0 : f - kKStages; i < f; ++i)
+        ptx::mbar_wait(&bars->k_full[i % kKStages], (i / kKStages) & 1);
+    }
+  } else if (warp == 10) {
+    // ================= TMA producer: the V tiles =================
+    if (lane == 0) {
+      int j = 0;
+      for (; j < n; ++j) {
+        const int st = j % kVStages;
+        if (j >= kVStages &&
+            !ptx::mbar_wait(&bars->v_empty[st], ((j / kVStages) - 1) & 1, fail)) {
+          atomicExch(const_cast<int *>(fail), 1);
+          break;
+        }
+        uint8_t *vd = smem + kOffV + st * kVStage;
+        ptx::mbar_arrive_expect_tx(&bars->v_full[st], kVStage);
+        ptx::tma_load_2d(vd, &tm_kv, &bars->v_full[st], xk + kDh, tok0 + j * kKT);
+        ptx::tma_load_2d(vd + kBox, &tm_kv, &bars->v_full[st], xk + kDh + 64, tok0 + j * kKT);
+      }
+      for (int i = j - kVStages < 0 ? 0 : j - kVStages; i < j; ++i)
+        ptx::mbar_wait(&bars->v_full[i % kVStages], (i / kVStages) & 1);
+    }
+  } else if (warp == 1 || warp == 11) {
+    // ======== MMA issuers: warp 1 Q K^T (and TMEM owner), warp 11 P V ========
+    // One thread cannot issue these MMAs at the tensor pipe's rate (its issue
+    // stalls while earlier MMAs execute); two threads, each waiting only on
+    // its own operands, keep the pipe fed.
+    if (lane == 0) {
       bool ok = true;
-      for (int j = 0; j < n; ++j) {
-        const int s = j & 1, y = tok0 + j * kKT;
-        if (j >= 2 && !ptx::mbar_wait(&bars->k_empty[s], ((j - 2) >> 1) & 1, fail)) {
-          ok = false;
-          break;
+      if (warp == 1) {
+        const uint32_t idesc_s = ptx::idesc_bf16(kQT, kKT, false, false);
+        const uint64_t kdesc =
+            ptx::smem_desc(ptx::smem_u32(smem + kOffK), 16, 1024, ptx::kSw128);
+        ok = ptx::mbar_wait(&bars->q_tmem, 0, fail);
+        ptx::tc_fence_after();
+        // the query's ring stage is free once every softmax warp has copied it
+        if (ok) ptx::mbar_arrive(&bars->k_empty[0]);
+        // S = Q K^T for key tile j (ring fill j + 1), A = the query in TMEM;
+        // tile j > 0 once the softmax has read tile j - 1's scores
+        for (int j = 0; j < n && ok; ++j) {
+          if (j > 0) {
+            if (!ptx::mbar_wait(&bars->s_free, (j - 1) & 1, fail)) {
+              ok = false;
+              break;
+            }
+          }
+          const int f = j + 1, st = f % kKStages;
+          if (!ptx::mbar_wait(&bars->k_full[st], (f / kKStages) & 1, fail)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint64_t kd = kdesc + (uint64_t)((st * kKStage) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < 12; ++kk) {  // 3 boxes x 4 k-steps of 16
+            const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
+            ptx::mma_bf16_ts(tmem + kTmemS, tmem + kTmemQ + kk * 8, kd + (uint64_t)(off >> 4),
+                             idesc_s, kk != 0);
+          }
+          ptx::mma_commit(&bars->s_full);
+          ptx::mma_commit(&bars->k_empty[st]);
         }
-        uint8_t *kd = smem + kOffK + s * kKStage;
-        ptx::mbar_arrive_expect_tx(&bars->k_full[s], kKStage);
-        ptx::tma_load_2d(kd, &tm_kv, &bars->k_full[s], xk, y);
-        ptx::tma_load_2d(kd + kBox, &tm_kv, &bars->k_full[s], xk + 64, y);
-        ptx::tma_load_2d(kd + 2 * kBox, &tm_kr, &bars->k_full[s], 0, y);
-        ++nk;
-        if (j >= 2 && !ptx::mbar_wait(&bars->v_empty[s], ((j - 2) >> 1) & 1, fail)) {
-          ok = false;
-          break;
+      } else {
+        const uint32_t idesc_o = ptx::idesc_bf16(kQT, kDh, false, true);
+        // V is MN-major: the two 64-wide d_v blocks are one box (kBox) apart
+        const uint64_t vdesc =
+            ptx::smem_desc(ptx::smem_u32(smem + kOffV), kBox, 1024, ptx::kSw128);
+        // O += P(j) V(j) once the softmax has written P(j)
+        for (int j = 0; j < n && ok; ++j) {
+          const int pb = j & 1, vs = j % kVStages;
+          if (!ptx::mbar_wait(&bars->p_full[pb], (j >> 1) & 1, fail) ||
+              !ptx::mbar_wait(&bars->v_full[vs], (j / kVStages) & 1, fail)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint64_t vd = vdesc + (uint64_t)((vs * kVStage) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < kKT / 16; ++kk)
+            ptx::mma_bf16_ts(tmem + kTmemO, tmem + kTmemP + pb * 64 + kk * 8,
+                             vd + (uint64_t)((kk * 2048) >> 4), idesc_o, (j | kk) != 0);
+          ptx::mma_commit(&bars->pv_done[pb]);
+          ptx::mma_commit(&bars->v_empty[vs]);
         }
-        uint8_t *vd = smem + kOffV + s * kVStage;
-        ptx::mbar_arrive_expect_tx(&bars->v_full[s], kVStage);
-        ptx::tma_load_2d(vd, &tm_kv, &bars->v_full[s], xk + kDh, y);
-        ptx::tma_load_2d(vd + kBox, &tm_kv, &bars->v_full[s], xk + kDh + 64, y);
-        ++nv;
+        if (ok) ptx::mma_commit(&bars->o_done);
       }
       if (!ok) atomicExch(const_cast<int *>(fail), 1);
-      // never leave with copies in flight: each ring's last fills have landed
-      ptx::mbar_wait(&bars->q_full, 0);
-      for (int j = nk - 2 < 0 ? 0 : nk - 2; j < nk; ++j)
-        ptx::mbar_wait(&bars->k_full[j & 1], (j >> 1) & 1);
-      for (int j = nv - 2 < 0 ? 0 : nv - 2; j < nv; ++j)
-        ptx::mbar_wait(&bars->v_full[j & 1], (j >> 1) & 1);
-    }
-  } else if (warp == 1) {
-    // ================= MMA issuer =================
-    if (lane == 0) {
-      const uint32_t idesc_s = ptx::idesc_bf16(kQT, kKT, false, false);
-      const uint32_t idesc_o = ptx::idesc_bf16(kQT, kDh, false, true);
-      const uint64_t qdesc = ptx::smem_desc(ptx::smem_u32(smem + kOffQ), 16, 1024, ptx::kSw128);
-      const uint64_t kdesc = ptx::smem_desc(ptx::smem_u32(smem + kOffK), 16, 1024, ptx::kSw128);
-      // V is MN-major: the two 64-wide d_v blocks are one box (kBox) apart
-      const uint64_t vdesc = ptx::smem_desc(ptx::smem_u32(smem + kOffV), kBox, 1024, ptx::kSw128);
-      auto issue_qk = [&](int j) -> bool {
-        const int s = j & 1;
-        if (!ptx::mbar_wait(&bars->k_full[s], (j >> 1) & 1, fail)) return false;
-        ptx::tc_fence_after();
-        const uint64_t kd = kdesc + (uint64_t)((s * kKStage) >> 4);
-#pragma unroll
-        for (int kk = 0; kk < 12; ++kk) {  // 3 boxes x 4 k-steps of 16
-          const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
-          ptx::mma_bf16(tmem + kTmemS + s * kKT, qdesc + (uint64_t)(off >> 4),
-                        kd + (uint64_t)(off >> 4), idesc_s, kk != 0);
-        }
-        ptx::mma_commit(&bars->s_full[s]);
-        ptx::mma_commit(&bars->k_empty[s]);
-        return true;
-      };
-      bool ok = ptx::mbar_wait(&bars->q_full, 0, fail);
-      ptx::tc_fence_after();
-      if (ok) ok = issue_qk(0);
-      if (ok && n > 1) ok = issue_qk(1);
-      for (int j = 0; j < n && ok; ++j) {
-        const int s = j & 1;
-        if (!ptx::mbar_wait(&bars->p_full[s], (j >> 1) & 1, fail) ||
-            !ptx::mbar_wait(&bars->v_full[s], (j >> 1) & 1, fail)) {
-          ok = false;
-          break;
-        }
-        ptx::tc_fence_after();
-        const uint64_t vd = vdesc + (uint64_t)((s * kVStage) >> 4);
-#pragma unroll
-        for (int kk = 0; kk < kKT / 16; ++kk)
-          ptx::mma_bf16_ts(tmem + kTmemO, tmem + kTmemP + s * 64 + kk * 8,
-                           vd + (uint64_t)((kk * 2048) >> 4), idesc_o, (j | kk) != 0);
-        ptx::mma_commit(&bars->pv_done[s]);
-        ptx::mma_commit(&bars->v_empty[s]);
-        if (j + 2 < n) ok = issue_qk(j + 2);
-      }
-      if (ok) ptx::mma_commit(&bars->o_done);
-      else atomicExch(const_cast<int *>(fail), 1);
-      // every MMA issued above has completed before TMEM is freed
-      ptx::mma_commit(&bars->drain);
-      ptx::mbar_wait(&bars->drain, 0);
+      // every MMA this thread issued has completed before TMEM is freed
+      uint64_t *dr = &bars->drain[warp == 1 ? 0 : 1];
+      ptx::mma_commit(dr);
+      ptx::mbar_wait(dr, 0);
     }
   } else {
-    // ================= softmax and epilogue (warps 2-5) =================
+    // ============ softmax and epilogue (warps 2-9, a pair per row quarter) ============
+    // warps w and w+4 share TMEM lanes 32*(w%4).. (one SM sub-partition) and
+    // split the 128 key columns of a tile, then the 128 output columns
     const int wq = warp & 3;
+    const int ch = (warp - 2) >> 2;  // column half
     const int row = wq * 32 + lane;  // query row of the tile = TMEM lane
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
-    const int q = q0 + row;                 // position in the sequence
-    const int qlim = q < T ? q : T - 1;     // last visible key (rows past T: all keys)
-    float m_used = -INFINITY, l = 0.f;
+    const int q = q0 + row;                // position in the sequence
+    const int qlim = q < T ? q : T - 1;    // last visible key (rows past T: all keys)
+    float *red = reinterpret_cast<float *>(smem + kOffRed);
+    // both warps of the pair arrive (release: the value written before is
+    // visible), then wait with a bounded wait
+    auto pair_exchange = [&](uint64_t *bar, uint32_t parity) -> bool {
+      ptx::mbar_arrive(bar);
+      return wait_warp(bar, parity, fail);
+    };
+    float m_used = -INFINITY, l = 0.f;  // m_used in scaled base-2 units
     bool ok = true;
-    for (int j = 0; j < n; ++j) {
+    // the query row into TMEM (A operand of Q K^T): from the ring's first
+    // stage, box b holding elements 64b.., its 16-byte chunk c of row r at
+    // (c ^ r%8); this warp takes three of the six 64-element halves-of-boxes
+    if (wait_warp(&bars->k_full[0], 0, fail)) {
+      const uint8_t *qrow = smem + kOffK + row * 128;
+#pragma unroll
+      for (int g = 0; g < 3; ++g) {
+        const int part = 3 * ch + g, bx = part >> 1, hh = part & 1;
+        uint32_t v[16];
+#pragma unroll
+        for (int c2 = 0; c2 < 4; ++c2) {
+          const int c = 4 * hh + c2;
+          const uint4 u = *reinterpret_cast<const uint4 *>(qrow + bx * kBox + ((c ^ (row & 7)) << 4));
+          v[4 * c2] = u.x;
+          v[4 * c2 + 1] = u.y;
+          v[4 * c2 + 2] = u.z;
+          v[4 * c2 + 3] = u.w;
+        }
+        ptx::tmem_st16_nc(tmem + lane_base + kTmemQ + bx * 32 + hh * 16, v);
+      }
+      ptx::tmem_st_wait();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&bars->q_tmem);
+    } else {
+      ok = false;
+    }
+    for (int j = 0; j < n && ok; ++j) {
       const int s = j & 1;
-      if (!wait_warp(&bars->s_full[s], (j >> 1) & 1, fail)) {
+      if (!wait_warp(&bars->s_full, j & 1, fail)) {
         ok = false;
         break;
       }
       ptx::tc_fence_after();
-      float x[kKT];
+      float x[64];
 #pragma unroll
-      for (int c = 0; c < kKT; c += 16) {
+      for (int c = 0; c < 64; c += 16) {
         float v[16];
-        ptx::tmem_ld16(tmem + lane_base + kTmemS + s * kKT + c, v);
+        ptx::tmem_ld16(tmem + lane_base + kTmemS + ch * 64 + c, v);
 #pragma unroll
         for (int i = 0; i < 16; ++i) x[c + i] = v[i];
       }
       ptx::tmem_ld_wait();
-      // base-2 logits; keys past this row's position are masked
-      const int lim = qlim - j * kKT;
-      float mt = -INFINITY;
+      // the score buffer may take the next tile now
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&bars->s_free);
+      if (j == n - 1) {
+        // the diagonal tile: keys past this row's position are masked (every
+        // key of an earlier tile precedes every query of this CTA)
+        const int lim = qlim - j * kKT - ch * 64;
 #pragma unroll
-      for (int c = 0; c < kKT; ++c) {
-        x[c] = c <= lim ? x[c] * a.scale_log2 : -INFINITY;
-        mt = fmaxf(mt, x[c]);
+        for (int c = 0; c < 64; ++c) x[c] = c <= lim ? x[c] : -INFINITY;
       }
+      float m4[4] = {x[0], x[1], x[2], x[3]};
+#pragma unroll
+      for (int c = 4; c < 64; c += 4)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) m4[i] = fmaxf(m4[i], x[c + i]);
+      float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+      // the pair's row maxima meet in shared memory (one buffer per tile
+      // parity, so a fast warp cannot overwrite a value its partner has yet
+      // to read)
+      red[(s * 2 + ch) * 128 + row] = mt;
+      if (!pair_exchange(&bars->pair_max[wq][s], (j >> 1) & 1)) {
+        ok = false;
+        break;
+      }
+      mt = fmaxf(mt, red[(s * 2 + (ch ^ 1)) * 128 + row]) * a.scale_log2;
       const bool grow = mt > m_used + kRescaleThreshold;
       float alpha = 1.f;
       if (grow) {
@@ -289,20 +395,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       l *= alpha;
       if (j > 0 && __any_sync(0xffffffffu, grow)) {
-        // O holds tiles 0 .. j-1: rescale this warp's rows once P(j-1) V is in
+        // O holds tiles 0 .. j-1: rescale this warp's rows and columns once
+        // P(j-1) V is in (both warps of the pair take the same decision)
         if (!wait_warp(&bars->pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, fail)) {
           ok = false;
           break;
         }
         ptx::tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < kDh; c += 16) {
+        for (int c = 0; c < 64; c += 16) {
           float v[16];
-          ptx::tmem_ld16(tmem + lane_base + kTmemO + c, v);
+          ptx::tmem_ld16(tmem + lane_base + kTmemO + ch * 64 + c, v);
           ptx::tmem_ld_wait();
 #pragma unroll
           for (int i = 0; i < 16; ++i) v[i] *= alpha;
-          ptx::tmem_st16(tmem + lane_base + kTmemO + c, v);
+          ptx::tmem_st16(tmem + lane_base + kTmemO + ch * 64 + c, v);
         }
       }
       // P buffer s was last read by P(j-2) V
@@ -311,24 +418,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       ptx::tc_fence_after();
-      float ls = 0.f;
+      const float nm = -m_used;
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c = 0; c < kKT; c += 32) {
+      for (int c = 0; c < 64; c += 32) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float p0 = ptx::ex2(x[c + 2 * i] - m_used);
-          const float p1 = ptx::ex2(x[c + 2 * i + 1] - m_used);
-          ls += p0 + p1;
+          const float p0 = ptx::ex2(fmaf(x[c + 2 * i], a.scale_log2, nm));
+          const float p1 = ptx::ex2(fmaf(x[c + 2 * i + 1], a.scale_log2, nm));
+          ls[i & 3] += p0 + p1;
           pk[i] = ptx::pack_bf16x2(p0, p1);
         }
-        ptx::tmem_st16_nc(tmem + lane_base + kTmemP + s * 64 + c / 2, pk);
+        ptx::tmem_st16_nc(tmem + lane_base + kTmemP + s * 64 + ch * 32 + c / 2, pk);
       }
-      l += ls;
+      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
       ptx::tmem_st_wait();
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&bars->p_full[s]);
+    }
+    // the pair's row sums
+    if (ok) {
+      red[(4 + ch) * 128 + row] = l;
+      if (pair_exchange(&bars->pair_sum[wq], 0)) l += red[(4 + (ch ^ 1)) * 128 + row];
+      else ok = false;
     }
     if (ok && !wait_warp(&bars->o_done, 0, fail)) ok = false;
     if (ok) {
@@ -337,20 +451,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float inv = 1.f / l;
       const size_t orow = (size_t)(tok0 + (store ? q : 0)) * a.H + h;
 #pragma unroll
-      for (int c = 0; c < kDh; c += 16) {
+      for (int c = 0; c < 64; c += 16) {
         float v[16];
-        ptx::tmem_ld16(tmem + lane_base + kTmemO + c, v);
+        ptx::tmem_ld16(tmem + lane_base + kTmemO + ch * 64 + c, v);
         ptx::tmem_ld_wait();
         uint32_t pk[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) pk[i] = ptx::pack_bf16x2(v[2 * i] * inv, v[2 * i + 1] * inv);
         if (store) {
-          uint4 *d4 = reinterpret_cast<uint4 *>(a.out + orow * kDh + c);
+          uint4 *d4 = reinterpret_cast<uint4 *>(a.out + orow * kDh + ch * 64 + c);
           d4[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
           d4[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
         }
       }
-      if (store) a.lse[orow] = (m_used + log2f(l)) * kLn2;
+      if (store && ch == 0) a.lse[orow] = (m_used + log2f(l)) * kLn2;
     } else {
       atomicExch(const_cast<int *>(fail), 1);
     }
@@ -402,7 +516,7 @@ struct RebuildArgs {
   int *err;
 };
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kRThreads, 1)
     kv_rebuild_kernel(const __grid_constant__ CUtensorMap tm_c,    // c_kv [T][512]
                       const __grid_constant__ CUtensorMap tm_wuk,  // W_UK [H*128][512]
                       const __grid_constant__ CUtensorMap tm_wuv,  // W_UV [H*128][512]
@@ -570,7 +684,7 @@ cudaError_t launch_kv_rebuild(const void *c_kv, const void *W_UK, const void *W_
   a.kv = static_cast<__nv_bfloat16 *>(kv);
   a.err = err;
   const dim3 grid((T + 127) / 128, (d.H + kRebuildHeads - 1) / kRebuildHeads);
-  kv_rebuild_kernel<<<grid, kThreads, kRSmemBytes, st>>>(tm_c, tm_wuk, tm_wuv, a);
+  kv_rebuild_kernel<<<grid, kRThreads, kRSmemBytes, st>>>(tm_c, tm_wuk, tm_wuv, a);
   return cudaGetLastError();
 }
 
