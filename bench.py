@@ -641,6 +641,20 @@ def run_reference(args, rank):
     }
 
 
+def run_prefill_only(args, device):
+    """``--prefill-only``: the prefill measurement alone (for profiling it)."""
+    import mla_latent_kv_74_b300 as mla
+    w = synth.WORKLOADS[args.workload]
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+    res = measure_prefill(mla, args, w, flush, stream, device)
+    if res is None:
+        return {"prefill": None, "why": f"no prefill path for the {w.name} workload's dims"}
+    return {"metric": "MLA prefill tensor TFLOP/s (K/V rebuild + causal attention)",
+            "value": res["tflops"], "unit": "TFLOP/s", "higher_is_better": True,
+            "dtype": "bf16", "data": "synthetic", "prefill": res}
+
+
 # ---------------------------------------------------------------------------
 
 
@@ -657,6 +671,8 @@ def main():
                     help="seconds of oracle work for the cpu_baseline key (0 = skip)")
     ap.add_argument("--ref-step-s", type=float, default=3.0,
                     help="seconds of oracle work per step of the reference arm")
+    ap.add_argument("--prefill-only", action="store_true",
+                    help="time only mla_prefill (four 4096-token prompts) and print its line")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -668,6 +684,13 @@ def main():
         res = run_reference(args, rank)
         if res is not None:
             print(json.dumps(res), flush=True)
+        return
+
+    if args.prefill_only:
+        if rank == 0:
+            device = torch.device("cuda", local_rank)
+            torch.cuda.set_device(device)
+            print(json.dumps(run_prefill_only(args, device)), flush=True)
         return
 
     if world > 1:
