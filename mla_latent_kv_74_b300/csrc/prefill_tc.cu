@@ -12,9 +12,13 @@
 // [K_nope | V] per (token, head) into the workspace, and prefill_attn_kernel
 // reads it.
 //
-// One CTA per (128-query tile, head, sequence); the query tiles of one head
-// are adjacent in the grid (heaviest first), so their shared K and V tiles
-// stay in L2 instead of being read from HBM once per query tile.
+// The attention kernel is persistent: one CTA per SM takes (128-query tile,
+// head, prompt) items from a work list in the workspace (a counter the
+// rebuild kernel zeroes).  Items are numbered with the query tiles of one
+// head adjacent (heaviest first), so the CTAs at work at any time share a
+// few heads' K and V in L2; each CTA loads the next item's query and first
+// key tiles, and computes its first scores, while it finishes the current
+// one.
 // Queries are the MMA M dimension (128 rows = TMEM lanes), keys come in
 // tiles of 128:
 //   S  = Q K^T    M=128, N=128, K=192  A = Q (TMEM), B = K tile (smem)
@@ -81,8 +85,17 @@ constexpr uint32_t kOffV = kOffK + kKStages * kKStage;
 constexpr uint32_t kOffRed = kOffV + kVStages * kVStage;
 constexpr uint32_t kOffBars = kOffRed + 6 * 128 * 4;
 
+// One unit of work: a 128-query tile of one head of one prompt (n key tiles;
+// n == 0 ends the list).
+struct Item {
+  int tok0, T, q0, h, n;
+};
+// roles that take each published item: the V producer, the two MMA issuers
+// (one thread each) and the eight softmax warps (one arrival per warp)
+constexpr uint32_t kItemTakers = 3 + 8;
+
 struct Bars {
-  uint64_t k_full[kKStages], k_empty[kKStages];  // K ring (fill 0: the query)
+  uint64_t k_full[kKStages], k_empty[kKStages];  // K ring: per item the query, then its key tiles
   uint64_t v_full[kVStages], v_empty[kVStages];  // V ring
   uint64_t q_tmem;      // the query copied into TMEM (one arrival per softmax warp)
   uint64_t s_full;      // scores of the current tile ready
@@ -94,6 +107,10 @@ struct Bars {
   // softmax pairs: row maxima of tile j exchanged (per row quarter and tile
   // parity), row sums exchanged at the end; 64 arrivals each
   uint64_t pair_max[4][2], pair_sum[4];
+  uint64_t o_free;  // the epilogue has read O (one arrival per softmax warp)
+  // the work list: warp 0 publishes each item, every other role takes it
+  uint64_t item_full[2], item_empty[2];
+  Item items[2];
   uint32_t tmem;
   int fail;
 };
@@ -108,6 +125,9 @@ constexpr uint32_t kTmemQ = 384;  // 96 (the 192 bf16 query elements of a row)
 struct PrefillArgs {
   const int32_t *cu_seqlens;  // [B + 1]
   int B, H, max_seqlen, total;
+  int nq;                           // query tiles per prompt at max_seqlen
+  unsigned long long total_items;   // B * H * nq
+  unsigned long long *next_item;    // work-list counter, zeroed by the rebuild kernel
   float scale_log2;
   __nv_bfloat16 *out;  // [total][H][128]
   float *lse;          // [total][H]
@@ -129,22 +149,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Bars *bars = reinterpret_cast<Bars *>(smem + kOffBars);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // query tiles vary fastest, so the CTAs that share one head's K and V run
-  // together and read them from L2; heaviest tiles first within each head
-  const int qt = (int)gridDim.x - 1 - (int)blockIdx.x;
-  const int h = blockIdx.y, b = blockIdx.z;
-
-  const int tok0 = a.cu_seqlens[b];
-  const int T = a.cu_seqlens[b + 1] - tok0;
-  if (tok0 < 0 || T < 0 || T > a.max_seqlen || tok0 > a.total - T) {
-    if (threadIdx.x == 0) set_device_error(a.err, kDevBounds);
-    return;
-  }
-  const int q0 = qt * kQT;
-  if (q0 >= T) return;
-  // key tiles 0 .. qt: the tile's first query sees key 128 qt, so every tile
-  // holds a visible key for every row
-  const int n = qt + 1;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kKStages; ++i) {
@@ -161,8 +165,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(&bars->p_full[i], 8);
       ptx::mbar_init(&bars->pv_done[i], 1);
+      ptx::mbar_init(&bars->item_full[i], 1);
+      ptx::mbar_init(&bars->item_empty[i], kItemTakers);
     }
     ptx::mbar_init(&bars->o_done, 1);
+    ptx::mbar_init(&bars->o_free, 8);
     ptx::mbar_init(&bars->drain[0], 1);
     ptx::mbar_init(&bars->drain[1], 1);
     for (int i = 0; i < 4; ++i) {
@@ -183,29 +190,83 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = bars->tmem;
   volatile int *fail = &bars->fail;
-  const int xk = h * 2 * kDh;  // column of this head's [K_nope | V] in the workspace
+  auto set_fail = [&]() { atomicExch(const_cast<int *>(fail), 1); };
+  // item k of this CTA's list, for the single-thread roles
+  auto take_item = [&](int k, Item *it) -> bool {
+    if (!ptx::mbar_wait(&bars->item_full[k & 1], (k >> 1) & 1, fail)) return false;
+    *it = bars->items[k & 1];
+    ptx::mbar_arrive(&bars->item_empty[k & 1]);
+    return true;
+  };
 
   if (warp == 0) {
-    // ================= TMA producer: the query, then the K tiles =================
+    // ======== work list and TMA producer: the query, then the K tiles ========
     if (lane == 0) {
-      ptx::mbar_arrive_expect_tx(&bars->k_full[0], kKStage);
-      ptx::tma_load_2d(smem + kOffK, &tm_q, &bars->k_full[0], h * kDh, tok0 + q0);
-      ptx::tma_load_2d(smem + kOffK + kBox, &tm_q, &bars->k_full[0], h * kDh + 64, tok0 + q0);
-      ptx::tma_load_2d(smem + kOffK + 2 * kBox, &tm_qr, &bars->k_full[0], h * kDr, tok0 + q0);
-      int f = 1;  // fill f of the ring is key tile f - 1
-      for (; f <= n; ++f) {
-        const int st = f % kKStages, y = tok0 + (f - 1) * kKT;
-        if (f >= kKStages &&
-            !ptx::mbar_wait(&bars->k_empty[st], ((f / kKStages) - 1) & 1, fail)) {
-          atomicExch(const_cast<int *>(fail), 1);
+      int f = 0;  // fills of the K ring (all items)
+      auto fill_wait = [&](int ff) -> bool {
+        return ff < kKStages ||
+               ptx::mbar_wait(&bars->k_empty[ff % kKStages], ((ff / kKStages) - 1) & 1, fail);
+      };
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        if (k >= 2 && !ptx::mbar_wait(&bars->item_empty[k & 1], ((k >> 1) - 1) & 1, fail)) {
+          ok = false;
           break;
         }
-        uint8_t *kd = smem + kOffK + st * kKStage;
-        ptx::mbar_arrive_expect_tx(&bars->k_full[st], kKStage);
-        ptx::tma_load_2d(kd, &tm_kv, &bars->k_full[st], xk, y);
-        ptx::tma_load_2d(kd + kBox, &tm_kv, &bars->k_full[st], xk + 64, y);
-        ptx::tma_load_2d(kd + 2 * kBox, &tm_kr, &bars->k_full[st], 0, y);
+        // the next non-empty (query tile, head, prompt), query tiles of one
+        // head adjacent and heaviest first, so the CTAs at work at any time
+        // share a few heads' K and V in L2
+        Item it = {0, 0, 0, 0, 0};
+        for (;;) {
+          const unsigned long long i = atomicAdd(a.next_item, 1ull);
+          if (i >= a.total_items) break;
+          const int qr = (int)(i % (unsigned long long)a.nq);
+          const unsigned long long rest = i / (unsigned long long)a.nq;
+          const int h = (int)(rest % (unsigned long long)a.H);
+          const int b = (int)(rest / (unsigned long long)a.H);
+          const int tok0 = a.cu_seqlens[b];
+          const int T = a.cu_seqlens[b + 1] - tok0;
+          if (tok0 < 0 || T < 0 || T > a.max_seqlen || tok0 > a.total - T) {
+            set_device_error(a.err, kDevBounds);
+            continue;
+          }
+          const int qt = a.nq - 1 - qr;
+          if (qt * kQT >= T) continue;
+          // key tiles 0 .. qt: the tile's first query sees key 128 qt, so
+          // every tile holds a visible key for every row
+          it = Item{tok0, T, qt * kQT, h, qt + 1};
+          break;
+        }
+        bars->items[k & 1] = it;
+        ptx::mbar_arrive(&bars->item_full[k & 1]);
+        if (it.n == 0) break;
+        if (!fill_wait(f)) {
+          ok = false;
+          break;
+        }
+        uint8_t *qd = smem + kOffK + (f % kKStages) * kKStage;
+        uint64_t *qb = &bars->k_full[f % kKStages];
+        ptx::mbar_arrive_expect_tx(qb, kKStage);
+        ptx::tma_load_2d(qd, &tm_q, qb, it.h * kDh, it.tok0 + it.q0);
+        ptx::tma_load_2d(qd + kBox, &tm_q, qb, it.h * kDh + 64, it.tok0 + it.q0);
+        ptx::tma_load_2d(qd + 2 * kBox, &tm_qr, qb, it.h * kDr, it.tok0 + it.q0);
+        ++f;
+        const int xk = it.h * 2 * kDh;
+        for (int j = 0; j < it.n; ++j, ++f) {
+          if (!fill_wait(f)) {
+            ok = false;
+            break;
+          }
+          uint8_t *kd = smem + kOffK + (f % kKStages) * kKStage;
+          uint64_t *kb = &bars->k_full[f % kKStages];
+          const int y = it.tok0 + j * kKT;
+          ptx::mbar_arrive_expect_tx(kb, kKStage);
+          ptx::tma_load_2d(kd, &tm_kv, kb, xk, y);
+          ptx::tma_load_2d(kd + kBox, &tm_kv, kb, xk + 64, y);
+          ptx::tma_load_2d(kd + 2 * kBox, &tm_kr, kb, 0, y);
+        }
       }
+      if (!ok) set_fail();
       // never leave with copies in flight: the ring's last fills have landed
       for (int i = f - kKStages < 0 ? 0 : f - kKStages; i < f; ++i)
         ptx::mbar_wait(&bars->k_full[i % kKStages], (i / kKStages) & 1);
@@ -213,20 +274,31 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 10) {
     // ================= TMA producer: the V tiles =================
     if (lane == 0) {
-      int j = 0;
-      for (; j < n; ++j) {
-        const int st = j % kVStages;
-        if (j >= kVStages &&
-            !ptx::mbar_wait(&bars->v_empty[st], ((j / kVStages) - 1) & 1, fail)) {
-          atomicExch(const_cast<int *>(fail), 1);
+      int fv = 0;
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        Item it;
+        if (!take_item(k, &it)) {
+          ok = false;
           break;
         }
-        uint8_t *vd = smem + kOffV + st * kVStage;
-        ptx::mbar_arrive_expect_tx(&bars->v_full[st], kVStage);
-        ptx::tma_load_2d(vd, &tm_kv, &bars->v_full[st], xk + kDh, tok0 + j * kKT);
-        ptx::tma_load_2d(vd + kBox, &tm_kv, &bars->v_full[st], xk + kDh + 64, tok0 + j * kKT);
+        if (it.n == 0) break;
+        const int xv = it.h * 2 * kDh + kDh;
+        for (int j = 0; j < it.n; ++j, ++fv) {
+          const int st = fv % kVStages;
+          if (fv >= kVStages &&
+              !ptx::mbar_wait(&bars->v_empty[st], ((fv / kVStages) - 1) & 1, fail)) {
+            ok = false;
+            break;
+          }
+          uint8_t *vd = smem + kOffV + st * kVStage;
+          ptx::mbar_arrive_expect_tx(&bars->v_full[st], kVStage);
+          ptx::tma_load_2d(vd, &tm_kv, &bars->v_full[st], xv, it.tok0 + j * kKT);
+          ptx::tma_load_2d(vd + kBox, &tm_kv, &bars->v_full[st], xv + 64, it.tok0 + j * kKT);
+        }
       }
-      for (int i = j - kVStages < 0 ? 0 : j - kVStages; i < j; ++i)
+      if (!ok) set_fail();
+      for (int i = fv - kVStages < 0 ? 0 : fv - kVStages; i < fv; ++i)
         ptx::mbar_wait(&bars->v_full[i % kVStages], (i / kVStages) & 1);
     }
   } else if (warp == 1 || warp == 11) {
@@ -240,60 +312,79 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t idesc_s = ptx::idesc_bf16(kQT, kKT, false, false);
         const uint64_t kdesc =
             ptx::smem_desc(ptx::smem_u32(smem + kOffK), 16, 1024, ptx::kSw128);
-        ok = ptx::mbar_wait(&bars->q_tmem, 0, fail);
-        ptx::tc_fence_after();
-        // the query's ring stage is free once every softmax warp has copied it
-        if (ok) ptx::mbar_arrive(&bars->k_empty[0]);
-        // S = Q K^T for key tile j (ring fill j + 1), A = the query in TMEM;
-        // tile j > 0 once the softmax has read tile j - 1's scores
-        for (int j = 0; j < n && ok; ++j) {
-          if (j > 0) {
-            if (!ptx::mbar_wait(&bars->s_free, (j - 1) & 1, fail)) {
-              ok = false;
-              break;
-            }
+        int f = 0, g = 0;  // K-ring fills, score tiles (all items)
+        for (int k = 0; ok; ++k) {
+          Item it;
+          if (!take_item(k, &it)) {
+            ok = false;
+            break;
           }
-          const int f = j + 1, st = f % kKStages;
-          if (!ptx::mbar_wait(&bars->k_full[st], (f / kKStages) & 1, fail)) {
+          if (it.n == 0) break;
+          // the item's query is in TMEM: its ring stage goes back
+          if (!ptx::mbar_wait(&bars->q_tmem, k & 1, fail)) {
             ok = false;
             break;
           }
           ptx::tc_fence_after();
-          const uint64_t kd = kdesc + (uint64_t)((st * kKStage) >> 4);
+          ptx::mbar_arrive(&bars->k_empty[f % kKStages]);
+          ++f;
+          // S = Q K^T per key tile, A = the query in TMEM, once the softmax
+          // has read the previous tile's scores
+          for (int j = 0; j < it.n; ++j, ++f, ++g) {
+            const int st = f % kKStages;
+            if ((g > 0 && !ptx::mbar_wait(&bars->s_free, (g - 1) & 1, fail)) ||
+                !ptx::mbar_wait(&bars->k_full[st], (f / kKStages) & 1, fail)) {
+              ok = false;
+              break;
+            }
+            ptx::tc_fence_after();
+            const uint64_t kd = kdesc + (uint64_t)((st * kKStage) >> 4);
 #pragma unroll
-          for (int kk = 0; kk < 12; ++kk) {  // 3 boxes x 4 k-steps of 16
-            const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
-            ptx::mma_bf16_ts(tmem + kTmemS, tmem + kTmemQ + kk * 8, kd + (uint64_t)(off >> 4),
-                             idesc_s, kk != 0);
+            for (int kk = 0; kk < 12; ++kk) {  // 3 boxes x 4 k-steps of 16
+              const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
+              ptx::mma_bf16_ts(tmem + kTmemS, tmem + kTmemQ + kk * 8, kd + (uint64_t)(off >> 4),
+                               idesc_s, kk != 0);
+            }
+            ptx::mma_commit(&bars->s_full);
+            ptx::mma_commit(&bars->k_empty[st]);
           }
-          ptx::mma_commit(&bars->s_full);
-          ptx::mma_commit(&bars->k_empty[st]);
         }
       } else {
         const uint32_t idesc_o = ptx::idesc_bf16(kQT, kDh, false, true);
         // V is MN-major: the two 64-wide d_v blocks are one box (kBox) apart
         const uint64_t vdesc =
             ptx::smem_desc(ptx::smem_u32(smem + kOffV), kBox, 1024, ptx::kSw128);
-        // O += P(j) V(j) once the softmax has written P(j)
-        for (int j = 0; j < n && ok; ++j) {
-          const int pb = j & 1, vs = j % kVStages;
-          if (!ptx::mbar_wait(&bars->p_full[pb], (j >> 1) & 1, fail) ||
-              !ptx::mbar_wait(&bars->v_full[vs], (j / kVStages) & 1, fail)) {
+        int g = 0;  // tiles (all items); V-ring fill = tile
+        for (int k = 0; ok; ++k) {
+          Item it;
+          if (!take_item(k, &it)) {
             ok = false;
             break;
           }
-          ptx::tc_fence_after();
-          const uint64_t vd = vdesc + (uint64_t)((vs * kVStage) >> 4);
+          if (it.n == 0) break;
+          // O += P(j) V(j) once the softmax has written P(j); the item's first
+          // tile starts O afresh once the previous item's epilogue read it
+          for (int j = 0; j < it.n; ++j, ++g) {
+            const int pb = g & 1, vs = g % kVStages;
+            if ((j == 0 && k > 0 && !ptx::mbar_wait(&bars->o_free, (k - 1) & 1, fail)) ||
+                !ptx::mbar_wait(&bars->p_full[pb], (g >> 1) & 1, fail) ||
+                !ptx::mbar_wait(&bars->v_full[vs], (g / kVStages) & 1, fail)) {
+              ok = false;
+              break;
+            }
+            ptx::tc_fence_after();
+            const uint64_t vd = vdesc + (uint64_t)((vs * kVStage) >> 4);
 #pragma unroll
-          for (int kk = 0; kk < kKT / 16; ++kk)
-            ptx::mma_bf16_ts(tmem + kTmemO, tmem + kTmemP + pb * 64 + kk * 8,
-                             vd + (uint64_t)((kk * 2048) >> 4), idesc_o, (j | kk) != 0);
-          ptx::mma_commit(&bars->pv_done[pb]);
-          ptx::mma_commit(&bars->v_empty[vs]);
+            for (int kk = 0; kk < kKT / 16; ++kk)
+              ptx::mma_bf16_ts(tmem + kTmemO, tmem + kTmemP + pb * 64 + kk * 8,
+                               vd + (uint64_t)((kk * 2048) >> 4), idesc_o, (j | kk) != 0);
+            ptx::mma_commit(&bars->pv_done[pb]);
+            ptx::mma_commit(&bars->v_empty[vs]);
+          }
+          if (ok) ptx::mma_commit(&bars->o_done);
         }
-        if (ok) ptx::mma_commit(&bars->o_done);
       }
-      if (!ok) atomicExch(const_cast<int *>(fail), 1);
+      if (!ok) set_fail();
       // every MMA this thread issued has completed before TMEM is freed
       uint64_t *dr = &bars->drain[warp == 1 ? 0 : 1];
       ptx::mma_commit(dr);
@@ -307,8 +398,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ch = (warp - 2) >> 2;  // column half
     const int row = wq * 32 + lane;  // query row of the tile = TMEM lane
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
-    const int q = q0 + row;                // position in the sequence
-    const int qlim = q < T ? q : T - 1;    // last visible key (rows past T: all keys)
     float *red = reinterpret_cast<float *>(smem + kOffRed);
     // both warps of the pair arrive (release: the value written before is
     // visible), then wait with a bounded wait
@@ -316,16 +405,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_arrive(bar);
       return wait_warp(bar, parity, fail);
     };
-    float m_used = -INFINITY, l = 0.f;  // m_used in scaled base-2 units
-    bool ok = true;
-    // the query row into TMEM (A operand of Q K^T): from the ring's first
-    // stage, box b holding elements 64b.., its 16-byte chunk c of row r at
-    // (c ^ r%8); this warp takes three of the six 64-element halves-of-boxes
-    if (wait_warp(&bars->k_full[0], 0, fail)) {
-      const uint8_t *qrow = smem + kOffK + row * 128;
+    auto take = [&](int k, Item *it) -> bool {
+      if (!wait_warp(&bars->item_full[k & 1], (k >> 1) & 1, fail)) return false;
+      *it = bars->items[k & 1];
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&bars->item_empty[k & 1]);
+      return true;
+    };
+    // the query rows of the item whose query is ring fill f, into TMEM (A
+    // operand of Q K^T): box b holds elements 64b.., its 16-byte chunk c of
+    // row r at (c ^ r%8); this warp takes three of the six 64-element
+    // halves-of-boxes
+    auto load_query = [&](int f) -> bool {
+      if (!wait_warp(&bars->k_full[f % kKStages], (f / kKStages) & 1, fail)) return false;
+      const uint8_t *qrow = smem + kOffK + (f % kKStages) * kKStage + row * 128;
 #pragma unroll
-      for (int g = 0; g < 3; ++g) {
-        const int part = 3 * ch + g, bx = part >> 1, hh = part & 1;
+      for (int gq = 0; gq < 3; ++gq) {
+        const int part = 3 * ch + gq, bx = part >> 1, hh = part & 1;
         uint32_t v[16];
 #pragma unroll
         for (int c2 = 0; c2 < 4; ++c2) {
@@ -342,114 +438,134 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&bars->q_tmem);
-    } else {
-      ok = false;
-    }
-    for (int j = 0; j < n && ok; ++j) {
-      const int s = j & 1;
-      if (!wait_warp(&bars->s_full, j & 1, fail)) {
-        ok = false;
-        break;
-      }
-      ptx::tc_fence_after();
-      float x[64];
-#pragma unroll
-      for (int c = 0; c < 64; c += 16) {
-        float v[16];
-        ptx::tmem_ld16(tmem + lane_base + kTmemS + ch * 64 + c, v);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) x[c + i] = v[i];
-      }
-      ptx::tmem_ld_wait();
-      // the score buffer may take the next tile now
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&bars->s_free);
-      if (j == n - 1) {
-        // the diagonal tile: keys past this row's position are masked (every
-        // key of an earlier tile precedes every query of this CTA)
-        const int lim = qlim - j * kKT - ch * 64;
-#pragma unroll
-        for (int c = 0; c < 64; ++c) x[c] = c <= lim ? x[c] : -INFINITY;
-      }
-      float m4[4] = {x[0], x[1], x[2], x[3]};
-#pragma unroll
-      for (int c = 4; c < 64; c += 4)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) m4[i] = fmaxf(m4[i], x[c + i]);
-      float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-      // the pair's row maxima meet in shared memory (one buffer per tile
-      // parity, so a fast warp cannot overwrite a value its partner has yet
-      // to read)
-      red[(s * 2 + ch) * 128 + row] = mt;
-      if (!pair_exchange(&bars->pair_max[wq][s], (j >> 1) & 1)) {
-        ok = false;
-        break;
-      }
-      mt = fmaxf(mt, red[(s * 2 + (ch ^ 1)) * 128 + row]) * a.scale_log2;
-      const bool grow = mt > m_used + kRescaleThreshold;
-      float alpha = 1.f;
-      if (grow) {
-        alpha = ptx::ex2(m_used - mt);  // 0 on the first tile (m_used = -inf)
-        m_used = mt;
-      }
-      l *= alpha;
-      if (j > 0 && __any_sync(0xffffffffu, grow)) {
-        // O holds tiles 0 .. j-1: rescale this warp's rows and columns once
-        // P(j-1) V is in (both warps of the pair take the same decision)
-        if (!wait_warp(&bars->pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, fail)) {
+      return true;
+    };
+    int f = 0, g = 0;  // K-ring fills, score tiles (all items)
+    Item it;
+    bool ok = take(0, &it) && (it.n == 0 || load_query(f));
+    for (int k = 0; ok && it.n > 0; ++k) {
+      const int n = it.n;
+      const int q = it.q0 + row;                    // position in the prompt
+      const int qlim = q < it.T ? q : it.T - 1;     // last visible key (rows past T: all keys)
+      float m_used = -INFINITY, l = 0.f;  // m_used in scaled base-2 units
+      for (int j = 0; j < n && ok; ++j, ++g) {
+        const int s = g & 1;
+        if (!wait_warp(&bars->s_full, g & 1, fail)) {
           ok = false;
           break;
         }
         ptx::tc_fence_after();
+        float x[64];
 #pragma unroll
         for (int c = 0; c < 64; c += 16) {
           float v[16];
-          ptx::tmem_ld16(tmem + lane_base + kTmemO + ch * 64 + c, v);
-          ptx::tmem_ld_wait();
+          ptx::tmem_ld16(tmem + lane_base + kTmemS + ch * 64 + c, v);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) v[i] *= alpha;
-          ptx::tmem_st16(tmem + lane_base + kTmemO + ch * 64 + c, v);
+          for (int i = 0; i < 16; ++i) x[c + i] = v[i];
         }
+        ptx::tmem_ld_wait();
+        // the score columns may take the next tile now
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&bars->s_free);
+        if (j == n - 1) {
+          // the diagonal tile: keys past this row's position are masked
+          // (every key of an earlier tile precedes every query of the item)
+          const int lim = qlim - j * kKT - ch * 64;
+#pragma unroll
+          for (int c = 0; c < 64; ++c) x[c] = c <= lim ? x[c] : -INFINITY;
+        }
+        float m4[4] = {x[0], x[1], x[2], x[3]};
+#pragma unroll
+        for (int c = 4; c < 64; c += 4)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) m4[i] = fmaxf(m4[i], x[c + i]);
+        float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+        // the pair's row maxima meet in shared memory (one buffer per tile
+        // parity, so a fast warp cannot overwrite a value its partner has
+        // yet to read)
+        red[(s * 2 + ch) * 128 + row] = mt;
+        if (!pair_exchange(&bars->pair_max[wq][s], (g >> 1) & 1)) {
+          ok = false;
+          break;
+        }
+        mt = fmaxf(mt, red[(s * 2 + (ch ^ 1)) * 128 + row]) * a.scale_log2;
+        const bool grow = mt > m_used + kRescaleThreshold;
+        float alpha = 1.f;
+        if (grow) {
+          alpha = ptx::ex2(m_used - mt);  // 0 on the item's first tile (m_used = -inf)
+          m_used = mt;
+        }
+        l *= alpha;
+        if (j > 0 && __any_sync(0xffffffffu, grow)) {
+          // O holds the item's tiles before this one: rescale this warp's
+          // rows and columns once the previous P V is in (both warps of the
+          // pair take the same decision)
+          if (!wait_warp(&bars->pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, fail)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < 64; c += 16) {
+            float v[16];
+            ptx::tmem_ld16(tmem + lane_base + kTmemO + ch * 64 + c, v);
+            ptx::tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] *= alpha;
+            ptx::tmem_st16(tmem + lane_base + kTmemO + ch * 64 + c, v);
+          }
+        }
+        // P buffer s was last read by the P V of tile g - 2
+        if (g >= 2 && !wait_warp(&bars->pv_done[s], ((g - 2) >> 1) & 1, fail)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const float nm = -m_used;
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int c = 0; c < 64; c += 32) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float p0 = ptx::ex2(fmaf(x[c + 2 * i], a.scale_log2, nm));
+            const float p1 = ptx::ex2(fmaf(x[c + 2 * i + 1], a.scale_log2, nm));
+            ls[i & 3] += p0 + p1;
+            pk[i] = ptx::pack_bf16x2(p0, p1);
+          }
+          ptx::tmem_st16_nc(tmem + lane_base + kTmemP + s * 64 + ch * 32 + c / 2, pk);
+        }
+        l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        ptx::tmem_st_wait();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&bars->p_full[s]);
       }
-      // P buffer s was last read by P(j-2) V
-      if (j >= 2 && !wait_warp(&bars->pv_done[s], ((j - 2) >> 1) & 1, fail)) {
+      if (!ok) break;
+      // the pair's row sums
+      red[(4 + ch) * 128 + row] = l;
+      if (!pair_exchange(&bars->pair_sum[wq], k & 1)) {
+        ok = false;
+        break;
+      }
+      l += red[(4 + (ch ^ 1)) * 128 + row];
+      // the next item's query goes into TMEM before this item's epilogue (every
+      // Q K^T of this item has completed), so its first Q K^T overlaps it
+      f += n + 1;
+      Item nx;
+      if (!take(k + 1, &nx) || (nx.n > 0 && !load_query(f))) {
+        ok = false;
+        break;
+      }
+      if (!wait_warp(&bars->o_done, k & 1, fail)) {
         ok = false;
         break;
       }
       ptx::tc_fence_after();
-      const float nm = -m_used;
-      float ls[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int c = 0; c < 64; c += 32) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float p0 = ptx::ex2(fmaf(x[c + 2 * i], a.scale_log2, nm));
-          const float p1 = ptx::ex2(fmaf(x[c + 2 * i + 1], a.scale_log2, nm));
-          ls[i & 3] += p0 + p1;
-          pk[i] = ptx::pack_bf16x2(p0, p1);
-        }
-        ptx::tmem_st16_nc(tmem + lane_base + kTmemP + s * 64 + ch * 32 + c / 2, pk);
-      }
-      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-      ptx::tmem_st_wait();
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&bars->p_full[s]);
-    }
-    // the pair's row sums
-    if (ok) {
-      red[(4 + ch) * 128 + row] = l;
-      if (pair_exchange(&bars->pair_sum[wq], 0)) l += red[(4 + (ch ^ 1)) * 128 + row];
-      else ok = false;
-    }
-    if (ok && !wait_warp(&bars->o_done, 0, fail)) ok = false;
-    if (ok) {
-      ptx::tc_fence_after();
-      const bool store = q < T;
+      const bool store = q < it.T;
       const float inv = 1.f / l;
-      const size_t orow = (size_t)(tok0 + (store ? q : 0)) * a.H + h;
+      const size_t orow = (size_t)(it.tok0 + (store ? q : 0)) * a.H + it.h;
 #pragma unroll
       for (int c = 0; c < 64; c += 16) {
         float v[16];
@@ -465,9 +581,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (store && ch == 0) a.lse[orow] = (m_used + log2f(l)) * kLn2;
-    } else {
-      atomicExch(const_cast<int *>(fail), 1);
+      // O may take the next item
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&bars->o_free);
+      it = nx;
     }
+    if (!ok) set_fail();
   }
 
   ptx::tc_fence_before();
@@ -514,6 +634,7 @@ struct RebuildArgs {
   int T, H;
   __nv_bfloat16 *kv;  // [T][H][256]
   int *err;
+  unsigned long long *next_item;  // the attention kernel's work-list counter, zeroed here
 };
 
 __global__ void __launch_bounds__(kRThreads, 1)
@@ -530,6 +651,8 @@ __global__ void __launch_bounds__(kRThreads, 1)
   const int h0 = blockIdx.y * kRebuildHeads;
   const int nh = a.H - h0 < kRebuildHeads ? a.H - h0 : kRebuildHeads;
   constexpr int kChunks = kDc / 64;
+  // the attention kernel that follows in the stream starts its work list at 0
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *a.next_item = 0;
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(&bars->a_full, 1);
@@ -665,7 +788,8 @@ __global__ void __launch_bounds__(kRThreads, 1)
 }
 
 cudaError_t launch_kv_rebuild(const void *c_kv, const void *W_UK, const void *W_UV, void *kv,
-                              int T, const mla_dims &d, int *err, cudaStream_t st) {
+                              int T, const mla_dims &d, int *err,
+                              unsigned long long *next_item, cudaStream_t st) {
   const uint64_t rows = (uint64_t)d.H * kDh;
   CUtensorMap tm_c, tm_wuk, tm_wuv;
   if (!make_tmap_2d_bf16(&tm_c, c_kv, kDc, T, kDc * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -683,6 +807,7 @@ cudaError_t launch_kv_rebuild(const void *c_kv, const void *W_UK, const void *W_
   a.H = d.H;
   a.kv = static_cast<__nv_bfloat16 *>(kv);
   a.err = err;
+  a.next_item = next_item;
   const dim3 grid((T + 127) / 128, (d.H + kRebuildHeads - 1) / kRebuildHeads);
   kv_rebuild_kernel<<<grid, kRThreads, kRSmemBytes, st>>>(tm_c, tm_wuk, tm_wuv, a);
   return cudaGetLastError();
@@ -706,8 +831,10 @@ cudaError_t launch_prefill_tc(const void *q_nope, const void *q_rope, const void
   char *ws = static_cast<char *>(workspace);
   void *kv = ws + kWsHeader;
   // [K_nope | V] of every (token, head): [total][H][256]
+  // workspace header: the error word at byte 0, the work-list counter at 8
+  unsigned long long *next_item = reinterpret_cast<unsigned long long *>(ws + 8);
   cudaError_t e = launch_kv_rebuild(c_kv, W_UK, W_UV, kv, total, d, reinterpret_cast<int *>(ws),
-                                    st);
+                                    next_item, st);
   if (e != cudaSuccess) return e;
   const uint64_t H = (uint64_t)d.H;
   CUtensorMap tm_q, tm_qr, tm_kv, tm_kr;
@@ -732,7 +859,17 @@ cudaError_t launch_prefill_tc(const void *q_nope, const void *q_rope, const void
   a.out = static_cast<__nv_bfloat16 *>(out);
   a.lse = lse;
   a.err = reinterpret_cast<int *>(ws);
-  const dim3 grid((max_seqlen + kQT - 1) / kQT, d.H, B);
+  a.nq = (max_seqlen + kQT - 1) / kQT;
+  a.total_items = (unsigned long long)B * d.H * a.nq;
+  a.next_item = next_item;
+  // persistent: one CTA per SM (shared memory and TMEM admit one), each
+  // taking (query tile, head, prompt) items from the work list
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+    return cudaErrorInvalidDevice;
+  const unsigned grid =
+      (unsigned)(a.total_items < (unsigned long long)sms ? a.total_items : (unsigned long long)sms);
   prefill_attn_kernel<<<grid, kThreads, kSmemBytes, st>>>(tm_q, tm_qr, tm_kv, tm_kr, a);
   return cudaGetLastError();
 }
