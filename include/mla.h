@@ -283,7 +283,9 @@ mla_status mla_prefill_workspace_size(int total_tokens, const mla_dims *dims,
  *   out         [total_tokens, H, d_h]             output
  *   lse         [total_tokens, H] float32          output
  *   workspace   >= mla_prefill_workspace_size bytes, 256-byte aligned; its
- *               first word is the error word that mla_get_error reads
+ *               first word is the error word that mla_get_error reads, its
+ *               bytes 8-15 the attention kernel's work-list counter (reset
+ *               by every call), the rest the rebuilt K and V
  * Supported: bf16, d_h = 128, d_c = 512, d_r = 64 (else MLA_ERR_UNSUPPORTED);
  * B <= 65535.  K and V are rounded to bf16 once after their fp32
  * accumulation; scores and the softmax are fp32, P is rounded to bf16 for
