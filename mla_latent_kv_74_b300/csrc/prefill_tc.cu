@@ -19,6 +19,7 @@
 // few heads' K and V in L2; each CTA loads the next item's query and first
 // key tiles, and computes its first scores, while it finishes the current
 // one.
+//
 // Queries are the MMA M dimension (128 rows = TMEM lanes), keys come in
 // tiles of 128:
 //   S  = Q K^T    M=128, N=128, K=192  A = Q (TMEM), B = K tile (smem)
@@ -32,14 +33,15 @@
 // and loaded by TMA.  Keeping the query out of shared memory buys the third
 // K stage, which hides the L2 latency of the next key tile.
 //
-// Warp roles (384 threads): warps 0 and 10 issue TMA (the query and the K
-// tiles; the V tiles), warp 1 owns TMEM and issues Q K^T, warp 11 issues
-// P V, warps 2-9 run the online softmax and the epilogue: thread = query row = TMEM lane, warps w
-// and w+4 on lanes 32*(w%4).. (one SM sub-partition), each taking half of a
-// tile's 128 key columns; the pair agrees on the row maximum through shared
-// memory and an mbarrier.  As soon as the softmax has read a score tile the
-// next Q K^T goes into the same columns, so the next scores are ready when
-// the softmax finishes; the P V of each tile follows its softmax.
+// Warp roles (384 threads): warp 0 runs the work list and loads the query
+// and K tiles, warp 10 loads the V tiles, warp 1 owns TMEM and issues
+// Q K^T, warp 11 issues P V, warps 2-9 run the online softmax and the
+// epilogue: thread = query row = TMEM lane, warps w and w+4 on lanes
+// 32*(w%4).. (one SM sub-partition), each taking half of a tile's 128 key
+// columns; the pair agrees on the row maximum through shared memory and an
+// mbarrier.  As soon as the softmax has read a score tile the next Q K^T
+// goes into the same columns, so the next scores are ready when the softmax
+// finishes; the P V of each tile follows its softmax.
 //
 // Online softmax in base 2 with lazy rescaling: the running maximum moves,
 // and the warp's rows of O are rescaled in TMEM, only when a tile's maximum
@@ -59,7 +61,7 @@
 namespace mla {
 namespace {
 
-constexpr int kQT = 128;  // queries per CTA
+constexpr int kQT = 128;  // queries per item (the MMA M dimension)
 constexpr int kKT = 128;  // keys per tile
 constexpr int kDh = 128, kDr = 64, kDc = 512;
 constexpr int kThreads = 384;   // attention: two TMA warps, two MMA warps, eight softmax warps
@@ -102,7 +104,7 @@ struct Bars {
   uint64_t s_free;      // ... and read (one arrival per softmax warp)
   uint64_t p_full[2];   // probabilities of tile j in buffer j % 2 (one arrival per warp)
   uint64_t pv_done[2];  // P(j) V accumulated (buffer j % 2 free again)
-  uint64_t o_done;
+  uint64_t o_done;    // the item's last P V accumulated
   uint64_t drain[2];  // each MMA issuer's last MMAs done
   // softmax pairs: row maxima of tile j exchanged (per row quarter and tile
   // parity), row sums exchanged at the end; 64 arrivals each
