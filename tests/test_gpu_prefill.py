@@ -79,6 +79,7 @@ SCALE = 1.0 / math.sqrt(128 + 64)
     ([300], 16),                 # three tiles, ragged tail
     ([5, 128, 129, 200], 8),     # packed; a sequence ending exactly on a tile
     ([3, 0, 250], 2),            # an empty sequence in the middle
+    ([130, 7], 12),              # a partial last group of heads in the rebuild
     ([1000], 128),               # all DeepSeek-V2 heads, eight tiles
 ])
 def test_prefill_matches_oracle(mla, seqlens, H):
