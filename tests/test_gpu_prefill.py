@@ -94,7 +94,8 @@ def test_prefill_matches_oracle(mla, seqlens, H):
 
 
 def test_prefill_max_seqlen_above_lengths(mla):
-    # a grid sized for longer sequences: the extra query tiles do nothing
+    # a work list sized for longer prompts: its query tiles past every
+    # prompt's end are skipped
     t = synth.prefill_tensors(seed=3, seqlens=[130, 60], H=4)
     got, glse, status = _run(mla, t, 4, max_seqlen=1000)
     assert status == mla.MLA_OK
