@@ -89,6 +89,16 @@ def gemm_work(w, B):
     return flops, bytes_
 
 
+def prefill_work(seqlens, H, d_h=128, d_r=64, d_c=512):
+    """Tensor FLOPs of mla_prefill: rebuilding [K_nope | V] (``2·T·H·2d_h·d_c``)
+    and the causal attention (``2·H·(d_h + d_r + d_h)`` per visible
+    (query, key) pair, ``T_b (T_b + 1) / 2`` pairs per prompt)."""
+    T = int(sum(seqlens))
+    kv = 2 * T * H * 2 * d_h * d_c
+    attn = sum(int(n) * (int(n) + 1) // 2 for n in seqlens) * 2 * H * (2 * d_h + d_r)
+    return kv, attn
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -468,8 +478,7 @@ def measure_prefill(mla, args, w, flush, stream, device):
                                              max(PREFILL_SEQLENS), dims, out, lse, ws,
                                              stream=stream),
                      max(3, min(args.steps, 20)), flush, stream)
-    kv_flops = 2 * T * w.H * 256 * 512
-    attn_flops = sum(n * (n + 1) // 2 for n in PREFILL_SEQLENS) * 2 * w.H * (128 + 64 + 128)
+    kv_flops, attn_flops = prefill_work(PREFILL_SEQLENS, w.H)
     peaks, _ = load_peaks()
     tflops = (kv_flops + attn_flops) / (ms * 1e-3) / 1e12
     return {
