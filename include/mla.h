@@ -308,6 +308,18 @@ mla_status mla_prefill(const void *q_nope, const void *q_rope, const void *c_kv,
  * Returns MLA_OK, MLA_ERR_DEVICE_BOUNDS, MLA_ERR_TIMEOUT or MLA_ERR_CUDA. */
 mla_status mla_get_error(void *workspace, mla_stream_t stream);
 
+/* Self-test of the failure path (no counterpart on the pages): one kernel
+ * waits, through the library's bounded wait, on an mbarrier phase that
+ * nothing completes.  The wait gives up after its limit (2 s) and the kernel
+ * records MLA_ERR_TIMEOUT in the workspace's error word, as a real lost wait
+ * in mla_decode or mla_prefill would.  mla_get_error then returns
+ * MLA_ERR_TIMEOUT and clears the word; the context stays usable.
+ *   workspace   any workspace of this library (>= 256 bytes, 256-byte
+ *               aligned); only its error word is written
+ * Returns MLA_ERR_WORKSPACE for a missing or misaligned workspace,
+ * MLA_ERR_CUDA if the launch fails. */
+mla_status mla_selftest_lost_wait(void *workspace, mla_stream_t stream);
+
 /* Static, human-readable name of a status code. */
 const char *mla_status_string(mla_status status);
 

@@ -57,6 +57,7 @@ EXPORTED = (
     "mla_project_query",
     "mla_prefill_workspace_size",
     "mla_prefill",
+    "mla_selftest_lost_wait",
 )
 
 # size of the scratch array built into the library for mla_decode_noalloc
@@ -110,6 +111,7 @@ def _load():
         "mla_project_query": [P, P, P, I, ctypes.c_float, P, I, I, D, P, P, P, Z, P],
         "mla_prefill_workspace_size": [I, D, ctypes.POINTER(Z)],
         "mla_prefill": [P, P, P, P, P, P, P, I, I, I, D, P, P, P, Z, P],
+        "mla_selftest_lost_wait": [P, P],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -288,6 +290,14 @@ def mla_prefill(q_nope, q_rope, c_kv, k_r, W_UK, W_UV, cu_seqlens, max_seqlen, d
                             _ptr(lse), _ptr(workspace),
                             workspace.numel() * workspace.element_size(), _stream(stream)),
            "mla_prefill")
+
+
+def mla_selftest_lost_wait(workspace, stream=None):
+    """Launch the failure-path self-test: a bounded wait that nothing
+    satisfies expires (after 2 s) and records MLA_ERR_TIMEOUT in
+    ``workspace``'s error word (read it with ``mla_get_error``)."""
+    _check(_lib.mla_selftest_lost_wait(_ptr(workspace), _stream(stream)),
+           "mla_selftest_lost_wait")
 
 
 def mla_get_error(workspace, stream=None) -> int:
