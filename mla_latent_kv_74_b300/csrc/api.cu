@@ -186,12 +186,10 @@ MLA_API mla_status mla_decode_workspace_size(int B, int Hq, int max_seqlen, cons
   if (!bytes) return MLA_ERR_INVALID_ARG;
   if (!dims_ok(dims)) return dims ? MLA_ERR_UNSUPPORTED : MLA_ERR_INVALID_ARG;
   if (B < 0 || Hq < 1 || max_seqlen < 0) return MLA_ERR_INVALID_ARG;
-  size_t s = simt_workspace_bytes(B, Hq, max_seqlen, *dims);
-  if (tc_decode_supported(*dims)) {
-    const size_t t = tc_decode_workspace_bytes(B, Hq, *dims);
-    if (t > s) s = t;
-  }
-  *bytes = s;
+  if ((long)B * Hq > kMaxDecodeItems) return MLA_ERR_UNSUPPORTED;
+  // only the path mla_decode takes for this problem
+  *bytes = tc_decode_supported(*dims, B, Hq) ? tc_decode_workspace_bytes(B, Hq, *dims)
+                                              : simt_workspace_bytes(B, Hq, max_seqlen, *dims);
   return MLA_OK;
 }
 
@@ -203,6 +201,7 @@ MLA_API mla_status mla_decode(const void *q_lat, const void *q_rope, const void 
   if (!dims_ok(dims)) return dims ? MLA_ERR_UNSUPPORTED : MLA_ERR_INVALID_ARG;
   if (B < 0 || Hq < 1 || max_seqlen < 0 || num_blocks < 1 || max_blocks < 1)
     return MLA_ERR_INVALID_ARG;
+  if ((long)B * Hq > kMaxDecodeItems) return MLA_ERR_UNSUPPORTED;
   if (B == 0) return MLA_OK;
   if (!q_lat || !cache || !block_table || !seqlens || !o_lat || !lse ||
       (dims->d_r > 0 && !q_rope))
@@ -216,7 +215,7 @@ MLA_API mla_status mla_decode(const void *q_lat, const void *q_rope, const void 
   if (workspace_bytes < need) return MLA_ERR_WORKSPACE;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const float scale = eff_scale(dims);
-  if (tc_decode_supported(*dims))
+  if (tc_decode_supported(*dims, B, Hq))
     return cuda_status(launch_decode_tc(q_lat, q_rope, cache, num_blocks, block_table,
                                         max_blocks, seqlens, max_seqlen, B, Hq, *dims, scale,
                                         o_lat, lse, workspace, st));

@@ -63,6 +63,8 @@
 // workspace, tells the peer CTA to stop, and the CTA unwinds (no trap).
 #include <math.h>
 
+#include <atomic>
+
 #include "internal.cuh"
 #include "ptx.cuh"
 #include "tc.cuh"
@@ -76,7 +78,9 @@ constexpr int kTile = 64;               // tokens per tile = block size
 constexpr int kDc = 512, kDr = 64, kD = kDc + kDr;
 constexpr int kStages = 3;
 constexpr int kThreads = 352;
-constexpr int kMaxItems = 1024;    // B * Hq limit of this path
+// B * Hq limit of this path: the plan's per-item scan uses the (still idle)
+// ring as scratch, 4 bytes per item
+constexpr int kMaxItems = 8192;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2(256)
@@ -152,6 +156,7 @@ constexpr int kEvRescale = 1, kEvEpilogue = 2, kEvDone = 3;
 constexpr uint32_t kOffMisc = kOffBars + ((sizeof(Bars) + 15) / 16) * 16;
 constexpr uint32_t kSmemBytes = kOffMisc + ((sizeof(Misc) + 15) / 16) * 16;
 static_assert(kSmemBytes <= 232448, "over the 227 KB shared-memory limit");
+static_assert((kMaxItems + 2) * 4 <= kStages * kSStage, "plan scan does not fit the ring");
 
 // TMEM columns
 constexpr uint32_t kTmemQ = 0;    // S: 288 columns of packed bf16 query
@@ -1177,9 +1182,13 @@ size_t part_bytes() { return align_up((size_t)2 * kMaxPairs * 128 * kDc * sizeof
 size_t lse_part_bytes() { return align_up((size_t)2 * kMaxPairs * 128 * sizeof(float), 256); }
 size_t plan_bytes(int B, int Hq) { return align_up(((size_t)B * Hq + 2) * sizeof(int), 256); }
 
+// Test hook: at most this many CTA pairs take part in the split plan (0:
+// no limit).  Set through mla_debug_set_decode_pairs.
+std::atomic<int> g_pairs_limit{0};
+
 // Co-resident clusters of two CTAs for this kernel (some GPCs may not fit a
 // whole number of pairs), capped at 74; looked up once per device.
-int pairs_for_device() {
+int pairs_on_device() {
   static int cached[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
@@ -1205,6 +1214,12 @@ int pairs_for_device() {
   return n;
 }
 
+int pairs_for_device() {
+  const int n = pairs_on_device();
+  const int limit = g_pairs_limit.load(std::memory_order_relaxed);
+  return (limit > 0 && limit < n) ? limit : n;
+}
+
 }  // namespace
 
 #ifdef MLA_TRACE
@@ -1220,9 +1235,13 @@ extern "C" __attribute__((visibility("default"))) int mla_debug_read_trace(void 
 }
 #endif
 
-bool tc_decode_supported(const mla_dims &d) {
+extern "C" __attribute__((visibility("default"))) int mla_debug_set_decode_pairs(int pairs) {
+  return g_pairs_limit.exchange(pairs > 0 ? pairs : 0);
+}
+
+bool tc_decode_supported(const mla_dims &d, int B, int Hq) {
   return d.dtype == MLA_BF16 && d.d_c == kDc && d.d_r == kDr && d.block_size == kTile &&
-         d.H <= 128;
+         d.H <= 128 && (long)B * Hq <= kMaxItems;
 }
 
 size_t tc_decode_workspace_bytes(int B, int Hq, const mla_dims &) {
@@ -1234,7 +1253,6 @@ cudaError_t launch_decode_tc(const void *q_lat, const void *q_rope, const void *
                              const int32_t *seqlens, int max_seqlen, int B, int Hq,
                              const mla_dims &d, float scale, void *o_lat, float *lse,
                              void *workspace, cudaStream_t st) {
-  if ((long)B * Hq > kMaxItems) return cudaErrorNotSupported;
   char *ws = static_cast<char *>(workspace);
   float *o_part = reinterpret_cast<float *>(ws + kWsHeader);
   const uint64_t rows = (uint64_t)B * Hq * d.H;

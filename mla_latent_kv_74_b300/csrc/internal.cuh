@@ -16,6 +16,9 @@ constexpr int kMaxDr = 64;    // d_r limit
 constexpr int kMaxDh = 128;   // d_h limit
 constexpr int kMaxH = 256;    // head limit
 constexpr int kNumSMs = 148;  // B300
+// B * Hq limit of mla_decode: the CUDA-core kernel's grid has one y index
+// per (sequence, query slot) item
+constexpr long kMaxDecodeItems = 65535;
 
 // Device error word values (the first int of the decode workspace).
 constexpr int kDevOk = 0;

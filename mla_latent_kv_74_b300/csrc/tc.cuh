@@ -7,8 +7,9 @@ namespace mla {
 
 // bf16, d_h = 128, d_c = 512 (per-head GEMMs on tcgen05).
 bool tc_gemm_supported(const mla_dims &d);
-// bf16, d_c = 512, d_r = 64, block_size = 64 (paged TMA decode on tcgen05).
-bool tc_decode_supported(const mla_dims &d);
+// bf16, d_c = 512, d_r = 64, block_size = 64, H <= 128 and at most 8192
+// (sequence, query slot) items (paged TMA decode on tcgen05).
+bool tc_decode_supported(const mla_dims &d, int B, int Hq);
 size_t tc_decode_workspace_bytes(int B, int Hq, const mla_dims &d);
 
 cudaError_t launch_absorb_tc(const void *q_nope, const void *W_UK, void *q_lat, int rows,

@@ -6,6 +6,7 @@ returns before touching CUDA, so they run on a machine without a GPU.
 """
 
 import ctypes
+import glob
 import os
 import re
 
@@ -17,9 +18,11 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 def _declared_symbols():
-    txt = open(os.path.join(ROOT, "include", "mla.h")).read()
-    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
-    return sorted(set(re.findall(r"\b(mla_[a-z_]+)\s*\(", txt)))
+    names = set()
+    for hdr in sorted(glob.glob(os.path.join(ROOT, "include", "*.h"))):
+        txt = re.sub(r"/\*.*?\*/", "", open(hdr).read(), flags=re.S)
+        names |= set(re.findall(r"\b(mla_[a-z_]+)\s*\(", txt))
+    return sorted(names)
 
 
 def test_library_builds_and_loads():
@@ -33,6 +36,12 @@ def test_every_declared_symbol_is_exported():
     lib = ctypes.CDLL(m.LIB_PATH)
     for name in declared:
         assert hasattr(lib, name), name
+
+
+def test_debug_pairs_limit_round_trips():
+    assert m.mla_debug_set_decode_pairs(7) == 0
+    assert m.mla_debug_set_decode_pairs(-3) == 7
+    assert m.mla_debug_set_decode_pairs(0) == 0
 
 
 def test_status_strings():
@@ -61,6 +70,42 @@ def test_workspace_size_validation():
     assert lib.mla_decode_workspace_size(64, 1, 8192, ctypes.byref(_dims()),
                                          ctypes.byref(n)) == m.MLA_OK
     assert n.value >= 256
+
+
+def test_decode_path_limits():
+    """The tensor-core decode takes at most 8192 (sequence, slot) items; larger
+    batches fall through to the CUDA-core kernel (whose workspace grows with
+    the rows), and more than 65535 items are refused before any launch."""
+    lib = m.raw_lib()
+    n = ctypes.c_size_t()
+    d = ctypes.byref(_dims())
+    assert lib.mla_decode_workspace_size(8192, 1, 64, d, ctypes.byref(n)) == m.MLA_OK
+    tc_bytes = n.value
+    assert tc_bytes < 48 << 20  # split partials of 74 CTA pairs, not of the rows
+    assert lib.mla_decode_workspace_size(8193, 1, 64, d, ctypes.byref(n)) == m.MLA_OK
+    assert n.value > 8193 * 128 * 512 * 4  # one fp32 partial row per (row, split)
+    assert lib.mla_decode_workspace_size(65536, 1, 64, d, ctypes.byref(n)) == \
+        m.MLA_ERR_UNSUPPORTED
+    assert lib.mla_decode_workspace_size(32768, 2, 64, d, ctypes.byref(n)) == \
+        m.MLA_ERR_UNSUPPORTED
+    ok = ctypes.c_void_p(1 << 20)
+    args = [ok, ok, ok, 4, ok, 4, ok, 64, 65536, 1, d, ok, ok, ok, 1 << 40, None]
+    assert lib.mla_decode(*args) == m.MLA_ERR_UNSUPPORTED
+    assert lib.mla_decode_noalloc(ok, ok, ok, 4, ok, 4, ok, 64, 65536, 1, d, ok, ok,
+                                  None) == m.MLA_ERR_UNSUPPORTED
+
+
+def test_noalloc_fits_every_tensor_core_workload():
+    """The built-in array of mla_decode_noalloc holds the workspace of each
+    DeepSeek-V2-shaped workload (the ragged two-slot one included), so none of
+    them is refused with MLA_ERR_WORKSPACE."""
+    lib = m.raw_lib()
+    n = ctypes.c_size_t()
+    for H, B, Hq, max_seqlen in ((16, 32, 1, 4096), (128, 64, 1, 8192), (128, 128, 2, 32768),
+                                 (128, 4, 1, 131072)):
+        assert lib.mla_decode_workspace_size(B, Hq, max_seqlen, ctypes.byref(_dims(H=H)),
+                                             ctypes.byref(n)) == m.MLA_OK
+        assert n.value <= m.NOALLOC_SCRATCH_BYTES, (H, B, Hq, n.value)
 
 
 @pytest.mark.parametrize("bad", [dict(H=0), dict(H=300), dict(d_h=256), dict(d_r=65),

@@ -175,14 +175,57 @@ def test_block_table_permutation_invariance(mla):
         assert np.array_equal(got[k], ref[k]), k
 
 
-def test_split_invariance(mla):
-    """A looser max_seqlen changes the split plan, not the result."""
-    inputs = synth.random_small(seed=9, H=128, seqlens=[1000, 333], Hq=1, **DS)
-    ref = run_gpu_step(mla, inputs)
-    for max_seqlen in (1000, 4096, 65536):
-        got = run_gpu_step(mla, inputs, max_seqlen=max_seqlen)
+def _pieces(seqlens, Hq, npairs, item_cost=6, tile=64):
+    """How many split pieces each (sequence, slot) item is cut into when its
+    tiles, each item preceded by ``item_cost`` start-up units, are laid end
+    to end and cut into ``npairs`` equal ranges (the tensor-core decode's
+    plan); used to show which piece counts a sweep covers."""
+    units, spans = 0, []
+    for n_seq in seqlens:
+        for i in range(Hq):
+            nt = -(-max(0, n_seq - Hq + i + 1) // tile)
+            if nt:
+                spans.append((units + item_cost, units + item_cost + nt))
+                units += item_cost + nt
+    per = -(-units // npairs)
+    return [(e - 1) // per - s // per + 1 for s, e in spans]
+
+
+SPLIT_CASES = {
+    "hq1": ([4000, 300, 64, 1, 900, 2500], 1),
+    "hq2": ([4500, 70, 5, 1400], 2),
+}
+
+
+@pytest.mark.parametrize("case", sorted(SPLIT_CASES))
+def test_split_invariance(mla, case):
+    """The result does not depend on how the items are cut between CTA pairs:
+    the pair count of the split plan is swept over 1, 3, 7 and every pair,
+    which cuts the longest item into 1, 2, 3 and about twenty pieces; every
+    sweep point matches the oracle, and the points match one another within
+    the rounding of the fp32 partials."""
+    seqlens, Hq = SPLIT_CASES[case]
+    inputs = synth.random_small(seed=9, H=128, seqlens=seqlens, Hq=Hq, **DS)
+    out, o_lat, lse, _ = run_oracle_step(inputs)
+    results = {}
+    covered = set()
+    try:
+        for npairs in (1, 3, 7, 74):
+            mla.mla_debug_set_decode_pairs(npairs)
+            covered.add(max(_pieces(seqlens, Hq, npairs)))
+            res = run_gpu_step(mla, inputs)
+            assert res["status"] == 0
+            compare(res["o_lat"], o_lat, f"o_lat pairs={npairs}")
+            compare(res["lse"], lse, f"lse pairs={npairs}")
+            compare(res["out"], out, f"out pairs={npairs}")
+            results[npairs] = res
+    finally:
+        mla.mla_debug_set_decode_pairs(0)
+    assert {1, 3}.issubset(covered) and max(covered) >= 10, covered
+    ref = results[1]
+    for npairs, res in results.items():
         for k in ("o_lat", "lse", "out"):
-            compare(got[k], ref[k], f"{k} max_seqlen={max_seqlen}")
+            compare(res[k], ref[k], f"{k} pairs={npairs} vs 1")
 
 
 def test_deterministic(mla):
@@ -221,3 +264,19 @@ def test_seqlen_above_max_reported(mla):
     # the error word is cleared by the read
     ws = mla.alloc_workspace(2, 1, 95, dims_for(mla, inputs))
     assert mla.mla_get_error(ws) == 0
+
+
+def test_many_items_fall_through_to_cuda_cores(mla):
+    """More (sequence, slot) items than the tensor-core plan takes (8192) run
+    on the CUDA-core kernel with the same results; sampled sequences are
+    compared with the oracle."""
+    g = np.random.default_rng(41)
+    seqlens = g.integers(1, 70, size=8200).tolist()
+    inputs = synth.random_small(seed=41, H=8, seqlens=seqlens, Hq=1, **DS)
+    res = run_gpu_step(mla, inputs)
+    assert res["status"] == 0
+    sample = [0, 1, 4095, 8191, 8192, 8199]
+    out, o_lat, lse, _ = run_oracle_step(inputs, sample)
+    compare(res["o_lat"][sample], o_lat, "o_lat")
+    compare(res["lse"][sample], lse, "lse")
+    compare(res["out"][sample], out, "out")
