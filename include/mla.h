@@ -44,11 +44,12 @@
  *   - Argument errors are detected on the host before anything is launched;
  *     the call then returns MLA_ERR_INVALID_ARG or MLA_ERR_UNSUPPORTED and
  *     leaves every buffer untouched.  A failed launch returns MLA_ERR_CUDA.
- *   - Errors found on the device (a block-table entry outside [0,num_blocks),
- *     a sequence length above max_seqlen or the table's capacity, a bounded
- *     wait that expired) are recorded in the decode workspace's error word;
- *     the affected rows are written as o_lat = 0, lse = -inf.  Read the word
- *     with mla_get_error.
+ *   - Errors found on the device are recorded in the decode workspace's
+ *     error word; read it with mla_get_error.  A block-table entry outside
+ *     [0,num_blocks) or a sequence length above max_seqlen or the table's
+ *     capacity (MLA_ERR_DEVICE_BOUNDS) leaves the affected rows written as
+ *     o_lat = 0, lse = -inf.  A bounded wait that expired (MLA_ERR_TIMEOUT)
+ *     stops the kernel early: rows it had not finished are left unwritten.
  *   - Positions start at 0.  seqlens[b] counts tokens AFTER the current Hq
  *     tokens were appended.  Query slot i (0 <= i < Hq) of sequence b sits
  *     at position seqlens[b]-Hq+i and sees positions 0..seqlens[b]-Hq+i
@@ -216,7 +217,9 @@ mla_status mla_o_proj(const void *out, const void *W_O, void *u, int B, int Hq,
  * workspace holds the split-KV partials, the split plan and the error word.
  * It must be zero-filled once before its first use; after that it may be
  * reused by consecutive calls on one stream.  max_seqlen is an upper bound
- * on seqlens[]. */
+ * on seqlens[].  The size is that of the path mla_decode takes for these
+ * arguments (see mla_decode).  B * Hq above 65535 returns
+ * MLA_ERR_UNSUPPORTED. */
 mla_status mla_decode_workspace_size(int B, int Hq, int max_seqlen,
                                      const mla_dims *dims, size_t *bytes);
 
@@ -237,7 +240,11 @@ mla_status mla_decode_workspace_size(int B, int Hq, int max_seqlen,
  *   o_lat       [B, Hq, H, d_c]                    output (dtype)
  *   lse         [B, Hq, H] float32                 output
  *   workspace   >= mla_decode_workspace_size bytes, 256-byte aligned
- * Consecutive calls that share a workspace must be ordered on one stream. */
+ * Consecutive calls that share a workspace must be ordered on one stream.
+ * Paths: bf16 with d_c = 512, d_r = 64, block_size = 64, H <= 128 and
+ * B * Hq <= 8192 runs on the tensor cores; every other supported problem
+ * with B * Hq <= 65535 on CUDA cores; B * Hq > 65535 returns
+ * MLA_ERR_UNSUPPORTED before anything is launched. */
 mla_status mla_decode(const void *q_lat, const void *q_rope, const void *cache,
                       int num_blocks, const int32_t *block_table,
                       int max_blocks, const int32_t *seqlens, int max_seqlen,
@@ -344,20 +351,32 @@ const char *mla_status_string(mla_status status);
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current) and caches it; make
  *     that first call before any stream capture.
+ *   - The array's device address is looked up (cudaGetSymbolAddress, with
+ *     the caller's device current) on every call; the lookup allocates
+ *     nothing.  The first call on a device, and the first after a device
+ *     reset, also loads the library onto that device: make it before any
+ *     stream capture.
  *   - All calls share the one array, which keeps the last call's contents;
  *     each call clears the part that must start at zero (the error word)
  *     before its kernels run.  Calls that overlap on the GPU (different
  *     streams, or different host threads without ordering) race on the array
  *     and give undefined results: order them on one stream.
- *   - Device-side errors are not reported through mla_get_error (the
- *     workspace is private); the affected rows still come back as o_lat = 0,
- *     lse = -inf. */
+ *   - Device-side errors go to the array's error word, with the effects
+ *     described for mla_decode; read them with mla_decode_noalloc_get_error
+ *     before the next call, which clears the word. */
 mla_status mla_decode_noalloc(const void *q_lat, const void *q_rope,
                               const void *cache, int num_blocks,
                               const int32_t *block_table, int max_blocks,
                               const int32_t *seqlens, int max_seqlen, int B,
                               int Hq, const mla_dims *dims, void *o_lat,
                               float *lse, mla_stream_t stream);
+
+/* mla_get_error for mla_decode_noalloc (no counterpart in the paper either):
+ * synchronise `stream`, then read and clear the error word of the built-in
+ * array (and the GEMMs' library-wide word, as mla_get_error does).  Returns
+ * MLA_OK, MLA_ERR_DEVICE_BOUNDS, MLA_ERR_TIMEOUT or MLA_ERR_CUDA.  It
+ * allocates nothing. */
+mla_status mla_decode_noalloc_get_error(mla_stream_t stream);
 
 #ifdef __cplusplus
 }

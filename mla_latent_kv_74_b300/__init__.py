@@ -39,7 +39,7 @@ MLA_ERR_TIMEOUT = 6
 MLA_BF16 = 0
 MLA_FP32 = 1
 
-# every symbol include/mla.h declares
+# every symbol include/mla.h and include/mla_debug.h declare
 EXPORTED = (
     "mla_absorb_query",
     "mla_append_cache",
@@ -49,6 +49,7 @@ EXPORTED = (
     "mla_get_error",
     "mla_status_string",
     "mla_decode_noalloc",
+    "mla_decode_noalloc_get_error",
     "mla_project_append_workspace_size",
     "mla_project_append",
     "mla_o_proj_workspace_size",
@@ -58,6 +59,7 @@ EXPORTED = (
     "mla_prefill_workspace_size",
     "mla_prefill",
     "mla_selftest_lost_wait",
+    "mla_debug_set_decode_pairs",
 )
 
 # size of the scratch array built into the library for mla_decode_noalloc
@@ -103,6 +105,7 @@ def _load():
         "mla_get_error": [P, P],
         "mla_status_string": [I],
         "mla_decode_noalloc": [P, P, P, I, P, I, P, I, I, I, D, P, P, P],
+        "mla_decode_noalloc_get_error": [P],
         "mla_project_append_workspace_size": [I, I, I, D, ctypes.POINTER(Z)],
         "mla_project_append": [P, P, P, I, ctypes.c_float, P, I, P, I, P, I, I, D, P, Z, P],
         "mla_o_proj_workspace_size": [I, I, I, D, ctypes.POINTER(Z)],
@@ -112,6 +115,7 @@ def _load():
         "mla_prefill_workspace_size": [I, D, ctypes.POINTER(Z)],
         "mla_prefill": [P, P, P, P, P, P, P, I, I, I, D, P, P, P, Z, P],
         "mla_selftest_lost_wait": [P, P],
+        "mla_debug_set_decode_pairs": [I],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -271,6 +275,12 @@ def mla_decode_noalloc(q_lat, q_rope, cache, num_blocks, block_table, seqlens, m
                                    _ptr(lse), _stream(stream)), "mla_decode_noalloc")
 
 
+def mla_decode_noalloc_get_error(stream=None) -> int:
+    """Synchronise, read and clear the built-in array's device error word
+    (the errors of ``mla_decode_noalloc``); returns the status."""
+    return int(_lib.mla_decode_noalloc_get_error(_stream(stream)))
+
+
 def mla_prefill_workspace_size(total_tokens, dims: Dims) -> int:
     n = ctypes.c_size_t(0)
     _check(_lib.mla_prefill_workspace_size(int(total_tokens), ctypes.byref(dims),
@@ -303,6 +313,13 @@ def mla_selftest_lost_wait(workspace, stream=None):
 def mla_get_error(workspace, stream=None) -> int:
     """Synchronise, read and clear the device error word; returns the status."""
     return int(_lib.mla_get_error(_ptr(workspace), _stream(stream)))
+
+
+def mla_debug_set_decode_pairs(pairs: int) -> int:
+    """Test hook (``include/mla_debug.h``): limit the CTA pairs of the
+    tensor-core decode's split plan (0 = no limit); returns the previous
+    limit."""
+    return int(_lib.mla_debug_set_decode_pairs(int(pairs)))
 
 
 def raw_lib():

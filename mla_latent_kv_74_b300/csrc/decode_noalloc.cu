@@ -11,10 +11,12 @@
 // library holds that array until the process exits.
 //
 // The array's name in host code is only a host-side stand-in for the symbol,
-// never a device address; the device address is looked up once per device
-// with cudaGetSymbolAddress (with that device current) and cached here.
-#include <mutex>
-
+// never a device address.  The device address is looked up with
+// cudaGetSymbolAddress, with the caller's device current, on every call: the
+// lookup allocates nothing, and a fresh lookup stays right after the device
+// or its primary context has been reset (which reloads the module and can
+// move the array).  The first lookup on a device loads the library's module
+// there, so that first call must not be made during stream capture.
 #include "internal.cuh"
 
 namespace mla {
@@ -24,23 +26,12 @@ constexpr size_t kNoAllocBytes = MLA_NOALLOC_SCRATCH_BYTES;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mu;
-void *g_scratch_ptr[kMaxDevices] = {};
-
-// Device address of the scratch array on the current device (looked up on
-// the first call made on that device).
+// Device address of the scratch array on the current device.
 mla_status scratch_for_current_device(void **out) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MLA_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
-    void *p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
-      return MLA_ERR_CUDA;
-    g_scratch_ptr[dev] = p;
-  }
-  *out = g_scratch_ptr[dev];
+  void *p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+    return MLA_ERR_CUDA;
+  *out = p;
   return MLA_OK;
 }
 
@@ -79,4 +70,14 @@ extern "C" __attribute__((visibility("default"))) mla_status mla_decode_noalloc(
   // 4. the regular decode, with the scratch array as its workspace
   return mla_decode(q_lat, q_rope, cache, num_blocks, block_table, max_blocks, seqlens,
                     max_seqlen, B, Hq, dims, o_lat, lse, scratch, kNoAllocBytes, stream);
+}
+
+extern "C" __attribute__((visibility("default"))) mla_status mla_decode_noalloc_get_error(
+    mla_stream_t stream) {
+  using namespace mla;
+  void *scratch = nullptr;
+  const mla_status t = scratch_for_current_device(&scratch);
+  if (t != MLA_OK) return t;
+  // the array's first 256 bytes are a decode workspace header like any other
+  return mla_get_error(scratch, stream);
 }

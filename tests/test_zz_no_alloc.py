@@ -12,6 +12,7 @@ cannot hide the rest of the suite.
 
 import ctypes
 
+
 import numpy as np
 import pytest
 import torch
@@ -91,3 +92,59 @@ def test_noalloc_rejects_oversized_problem(mla):
     status = mla.raw_lib().mla_decode_noalloc(p, p, p, 1, p, 1, p, max_seqlen, B, Hq,
                                               ctypes.byref(dims), p, p, None)
     assert status == mla.MLA_ERR_WORKSPACE
+
+
+def _noalloc(mla, dev, inputs, q_lat, dims, o, lse):
+    return mla.raw_lib().mla_decode_noalloc(
+        q_lat.data_ptr(), dev["q_rope"].data_ptr(), dev["cache"].data_ptr(), inputs["num_blocks"],
+        dev["block_table"].data_ptr(), dev["block_table"].shape[1], dev["seqlens"].data_ptr(),
+        int(inputs["seqlens"].max()), q_lat.shape[0], q_lat.shape[1], ctypes.byref(dims),
+        o.data_ptr(), lse.data_ptr(), torch.cuda.current_stream().cuda_stream)
+
+
+def test_noalloc_reports_device_errors_then_recovers(mla):
+    """A block-table entry outside [0, num_blocks) is caught on the device:
+    mla_decode_noalloc_get_error returns MLA_ERR_DEVICE_BOUNDS (and clears it),
+    that sequence's rows come back as o_lat = 0, lse = -inf, the other
+    sequence is unaffected, and the next clean call through the same shared
+    array matches mla_decode again."""
+    inputs = synth.random_small(seed=34, H=128, d_h=128, d_c=512, d_r=64, seqlens=[130, 200],
+                                Hq=1)
+    dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inputs.items()}
+    dims = mla.Dims(H=128, d_h=128, d_c=512, d_r=64, block_size=64, dtype=torch.bfloat16)
+    q_lat = torch.empty(2, 1, 128, 512, dtype=torch.bfloat16, device="cuda")
+    mla.mla_absorb_query(dev["q_nope"], dev["W_UK"], q_lat, dims)
+    ws = mla.alloc_workspace(2, 1, int(inputs["seqlens"].max()), dims)
+    o_ref = torch.empty_like(q_lat)
+    lse_ref = torch.empty(2, 1, 128, dtype=torch.float32, device="cuda")
+    mla.mla_decode(q_lat, dev["q_rope"], dev["cache"], inputs["num_blocks"], dev["block_table"],
+                   dev["seqlens"], int(inputs["seqlens"].max()), dims, o_ref, lse_ref, ws)
+    assert mla.mla_get_error(ws) == mla.MLA_OK
+
+    bad = dict(dev)
+    bt = dev["block_table"].clone()
+    bt[1, 1] = inputs["num_blocks"] + 7
+    bad["block_table"] = bt
+    o = torch.full_like(q_lat, float("nan"))
+    lse = torch.full((2, 1, 128), float("nan"), dtype=torch.float32, device="cuda")
+    assert _noalloc(mla, bad, inputs, q_lat, dims, o, lse) == mla.MLA_OK
+    assert mla.mla_decode_noalloc_get_error() == mla.MLA_ERR_DEVICE_BOUNDS
+    assert mla.mla_decode_noalloc_get_error() == mla.MLA_OK  # read and cleared
+    o_h, lse_h = o.float().cpu().numpy(), lse.cpu().numpy()
+    assert np.all(o_h[1] == 0) and np.all(np.isneginf(lse_h[1]))
+    assert np.array_equal(o_h[0], o_ref.float().cpu().numpy()[0])
+    assert np.array_equal(lse_h[0], lse_ref.cpu().numpy()[0])
+
+    o2 = torch.full_like(q_lat, float("nan"))
+    lse2 = torch.full((2, 1, 128), float("nan"), dtype=torch.float32, device="cuda")
+    assert _noalloc(mla, dev, inputs, q_lat, dims, o2, lse2) == mla.MLA_OK
+    assert mla.mla_decode_noalloc_get_error() == mla.MLA_OK
+    compare(o2.float().cpu().numpy(), o_ref.float().cpu().numpy(), "o_lat after an error", "bf16")
+    compare(lse2.cpu().numpy(), lse_ref.cpu().numpy(), "lse after an error", "bf16")
+
+
+def test_noalloc_takes_the_ragged_two_slot_shape(mla):
+    """The workspace of the ragged two-slot workload (B = 128, Hq = 2,
+    max_seqlen 32768, H = 128) fits the built-in array."""
+    dims = mla.Dims(H=128, d_h=128, d_c=512, d_r=64, block_size=64, dtype=torch.bfloat16)
+    assert mla.mla_decode_workspace_size(128, 2, 32768, dims) <= mla.NOALLOC_SCRATCH_BYTES
