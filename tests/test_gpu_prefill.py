@@ -20,7 +20,8 @@ from oracle import prefill as opf
 
 pytestmark = pytest.mark.gpu
 
-MAX_ABS = 2 * 2.0 ** -6
+# the decode step's tolerances (bf16 inputs, fp32 accumulation)
+MAX_ABS = 2e-2
 MEAN_REL = 5e-3
 LSE_ABS = 1e-2  # lse is fp32; the scores carry the rounding of K
 
