@@ -11,9 +11,10 @@ Timing: W untimed warm-up steps, then K steps.  Before every timed step L2
 is flushed by writing a 256 MiB buffer (outside the step's events); each
 step is timed with CUDA events on the stream the library launches on.  The
 mla_decode call is also timed on its own: that is the kernel the roofline
-fraction describes.  N > 1 (torchrun): every rank runs its own replica of
-the workload (weak scaling, no collective on the data path); rank 0 reports
-the max over ranks and the whole-job throughput.
+fraction describes.  N > 1 (under torchrun, or ``--gpus N`` alone, which
+starts the N rank processes itself): every rank runs its own replica of the
+workload on its own GPU (weak scaling, no collective on the data path); rank
+0 reports the max over ranks and the whole-job throughput.
 """
 
 from __future__ import annotations
@@ -271,6 +272,9 @@ def run_ours(args, rank, world, device):
         if it >= args.warmup:
             e2e_ms.append(e0.elapsed_time(e1))
 
+    # ---- the other decode workloads (mla_decode alone) -------------------------
+    configs = measure_other_configs(mla, args, flush, stream, device) if rank == 0 else None
+
     # ---- the fused projection-and-append step (measured on its own) ---------
     proj = measure_project_append(mla, args, w, dev, inp, dims, flush, stream, device)
     oproj = measure_o_proj(mla, args, w, out, dims, flush, stream, device)
@@ -321,7 +325,8 @@ def run_ours(args, rank, world, device):
             "visible_tokens": visible_tokens(seqlens, w.Hq),
             "step": "append + absorb + decode(split-KV + combine) + out_proj",
             "l2": "flushed before every timed step (256 MiB write outside the step's events)",
-            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "parallelism": (f"dp{world}: one replica of the workload per GPU (weak scaling, "
+                            "no collective on the data path)") if world > 1 else "single GPU",
         },
         "decode": {
             "ms": round(t_dec, 5),
@@ -355,6 +360,8 @@ def run_ours(args, rank, world, device):
         "clocks": clocks.summary(),
         "wall_s_timed_region": round(t_wall, 3),
     }
+    if configs:
+        res["configs"] = configs
     if proj is not None:
         res["project_append"] = proj
     if oproj is not None:
@@ -364,6 +371,61 @@ def run_ours(args, rank, world, device):
     if pre is not None:
         res["prefill"] = pre
     return res
+
+
+# workloads whose mla_decode is measured beside the step's (tiny is a
+# parity case: launch-bound, nothing to fraction)
+OTHER_CONFIGS = ("lite", "mtp", "long")
+
+
+def measure_other_configs(mla, args, flush, stream, device):
+    """``mla_decode`` alone on each of the other workloads, with its own
+    inputs (the same seeded recipe as the parity tests), L2 flushed before
+    every call: time, cache GB/s, TFLOP/s and the fraction of
+    ``max(bytes / HBM, FLOPs / bf16 peak)``, the same roofline as the step's."""
+    peaks, _ = load_peaks()
+    out = {}
+    for name in OTHER_CONFIGS:
+        if name == args.workload:
+            continue
+        inp, dev = setup_inputs(name, device)
+        w = inp["workload"]
+        seqlens = inp["seqlens"].numpy()
+        max_seqlen = int(seqlens.max())
+        dims = mla.Dims(H=w.H, d_h=w.d_h, d_c=w.d_c, d_r=w.d_r, block_size=w.block_size,
+                        dtype=torch.bfloat16)
+        q_lat = torch.empty(w.B, w.Hq, w.H, w.d_c, dtype=torch.bfloat16, device=device)
+        mla.mla_absorb_query(dev["q_nope"], dev["W_UK"], q_lat, dims, stream)
+        o_lat = torch.empty_like(q_lat)
+        lse = torch.empty(w.B, w.Hq, w.H, dtype=torch.float32, device=device)
+        ws = mla.alloc_workspace(w.B, w.Hq, max_seqlen, dims, device=device)
+
+        def call():
+            mla.mla_decode(q_lat, dev["q_rope"], dev["cache"], inp["num_blocks"],
+                           dev["block_table"], dev["seqlens"], max_seqlen, dims, o_lat, lse, ws,
+                           stream)
+
+        ms = _time_calls(call, max(3, min(args.steps, 20)), flush, stream)
+        status = mla.mla_get_error(ws)
+        if status != 0:
+            raise RuntimeError(f"{name}: device error {mla.status_string(status)}")
+        flops, nbytes = decode_work(w, seqlens)
+        t_mem, t_tc = nbytes / (peaks["hbm_gbs"] * 1e9), flops / (peaks["bf16_tflops"] * 1e12)
+        out[name] = {
+            "workload": synth.DESCRIPTIONS[name],
+            "ms": round(ms, 5),
+            "cache_gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
+            "tflops": round(flops / (ms * 1e-3) / 1e12, 2),
+            "bound": "hbm" if t_mem >= t_tc else "tensor",
+            "roofline_time_ms": round(max(t_mem, t_tc) * 1e3, 5),
+            "roofline_time_frac": round(max(t_mem, t_tc) / (ms * 1e-3), 4),
+            "algorithmic_flops": flops,
+            "algorithmic_bytes": nbytes,
+            "traffic": load_traffic(name),
+        }
+        del inp, dev, q_lat, o_lat, lse, ws
+        torch.cuda.empty_cache()
+    return out
 
 
 # hidden size of the model each workload is shaped after (DeepSeek-V2: 5120,
@@ -667,6 +729,31 @@ def run_prefill_only(args, device):
 # ---------------------------------------------------------------------------
 
 
+def spawn_ranks(n, cmd=None):
+    """Run ``n`` ranks of this benchmark on this node, one process per GPU,
+    when it was started without torchrun: child r gets RANK = LOCAL_RANK = r,
+    WORLD_SIZE = n and a rendezvous on 127.0.0.1.  ``cmd`` (default: this
+    script with the same arguments) is the child command line.  Returns the
+    first non-zero exit code of the children, else 0."""
+    import socket
+
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    if cmd is None:
+        cmd = [sys.executable, os.path.abspath(__file__), *sys.argv[1:]]
+    procs = []
+    for r in range(n):
+        env = dict(os.environ, RANK=str(r), LOCAL_RANK=str(r), WORLD_SIZE=str(n),
+                   MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+        procs.append(subprocess.Popen(cmd, env=env))
+    rc = 0
+    for proc in procs:
+        code = proc.wait()
+        rc = rc or code
+    return rc
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -685,6 +772,9 @@ def main():
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        # not under torchrun: one process per GPU, started here
+        sys.exit(spawn_ranks(args.gpus))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))

@@ -19,6 +19,9 @@ __global__ void __launch_bounds__(128) append_kernel(T *__restrict__ cache, int 
                                                      const T *__restrict__ c_kv,
                                                      const T *__restrict__ k_r, int n_new,
                                                      int d_c, int d_r, int bs, bool vec) {
+  // the next kernel of the step may launch now: it waits for this grid's
+  // completion before it reads anything this grid writes
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int i = blockIdx.x;  // new-token index
   const int b = blockIdx.y;
   const int pos = seqlens[b] - n_new + i;

@@ -1063,8 +1063,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 constexpr int kCombineRows = 8;
 __global__ void __launch_bounds__(32 * kCombineRows) combine_tc_kernel(DecodeArgs a) {
   // launched early, behind the decode grid: its pieces are complete and
-  // visible only after this wait
+  // visible only after this wait; the next kernel may launch after it
   ptx::grid_dependency_wait();
+  ptx::launch_dependents();
 #ifdef MLA_TRACE
   if (threadIdx.x == 0) atomicMin(&g_trace_comb[0], ptx::globaltimer_ns());
   struct CombEnd {

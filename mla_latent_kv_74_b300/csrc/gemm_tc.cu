@@ -26,6 +26,13 @@
 // accumulator (warp w reads TMEM lanes 32w..32w+31).  K is streamed in
 // 64-wide chunks through a ring of shared-memory stages (full / empty
 // mbarriers).
+//
+// The kernels are launched as programmatic dependents of the previous kernel
+// in the stream.  The producer first issues the weight tiles of every stage
+// (no kernel of this library writes weights), then waits for the previous
+// kernel to complete before it reads the activations, so the weight stream
+// overlaps the tail of the previous kernel; it lets the next kernel launch
+// only after that wait.
 #include "internal.cuh"
 #include "ptx.cuh"
 #include "tc.cuh"
@@ -38,7 +45,7 @@ __device__ int g_gemm_error = 0;
 
 constexpr int kM = 128;
 constexpr int kKChunk = 64;  // one 128-byte swizzle span of bf16
-constexpr int kMaxStages = 4;
+constexpr int kMaxStages = 8;
 constexpr uint32_t kABytes = kM * kKChunk * 2;  // 16 KB per chunk
 
 struct GemmArgs {
@@ -77,6 +84,7 @@ __global__ void __launch_bounds__(128, 1)
 
   const int warp = threadIdx.x >> 5;
   const int m0 = blockIdx.x * kM;
+  const int npre = g.num_k_chunks < g.stages ? g.num_k_chunks : g.stages;
   const int h = blockIdx.y;
   const int n0 = blockIdx.z * g.Nt;
   const uint32_t ncols = g.Nt <= 32 ? 32 : (g.Nt <= 64 ? 64 : (g.Nt <= 128 ? 128 : 256));
@@ -98,25 +106,14 @@ __global__ void __launch_bounds__(128, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = tmem_base;
-  // a programmatic dependent launched next may be scheduled now (it waits
-  // for this grid's completion before reading anything this grid writes)
-  ptx::launch_dependents();
 
   if (warp == 0 && ptx::elect_lane0()) {
     // ---- TMA producer ----
     const bool second = (int)blockIdx.x >= g.a_tiles;
     const CUtensorMap *ta = second ? &tmA2 : &tmA;
     const int am0 = second ? ((int)blockIdx.x - g.a_tiles) * kM : m0;
-    int issued = 0;
-    for (int k = 0; k < g.num_k_chunks; ++k) {
-      const int s = k % g.stages;
-      if (k >= g.stages && !ptx::mbar_wait(&empty[s], ((k / g.stages) - 1) & 1, &fail)) {
-        atomicExch(&fail, 1);
-        break;
-      }
+    auto load_a = [&](int k, int s) {
       uint8_t *a_dst = smem + s * stage_bytes;
-      uint8_t *b_dst = a_dst + kABytes;
-      ptx::mbar_arrive_expect_tx(&full[s], stage_bytes);
       if (kAMnMajor) {
         // two 64(M) x 64(K) boxes: M block j at +8 KB
         ptx::tma_load_2d(a_dst, ta, &full[s], am0, h * g.a_rows_per_head + k * kKChunk);
@@ -126,7 +123,29 @@ __global__ void __launch_bounds__(128, 1)
         ptx::tma_load_2d(a_dst, ta, &full[s], h * g.a_cols_per_head + k * kKChunk,
                          h * g.a_rows_per_head + am0);
       }
-      ptx::tma_load_2d(b_dst, &tmB, &full[s], h * g.b_cols_per_head + k * kKChunk, n0);
+    };
+    auto load_b = [&](int k, int s) {
+      ptx::tma_load_2d(smem + s * stage_bytes + kABytes, &tmB, &full[s],
+                       h * g.b_cols_per_head + k * kKChunk, n0);
+    };
+    // the weights of the first stages do not depend on the previous kernel
+    for (int k = 0; k < npre; ++k) {
+      ptx::mbar_arrive_expect_tx(&full[k], stage_bytes);  // A now, B below
+      load_a(k, k);
+    }
+    ptx::grid_dependency_wait();  // the activations may come from the previous kernel
+    ptx::launch_dependents();
+    for (int k = 0; k < npre; ++k) load_b(k, k);
+    int issued = npre;
+    for (int k = npre; k < g.num_k_chunks; ++k) {
+      const int s = k % g.stages;
+      if (!ptx::mbar_wait(&empty[s], ((k / g.stages) - 1) & 1, &fail)) {
+        atomicExch(&fail, 1);
+        break;
+      }
+      ptx::mbar_arrive_expect_tx(&full[s], stage_bytes);
+      load_a(k, s);
+      load_b(k, s);
       ++issued;
     }
     // never leave with copies in flight
@@ -201,18 +220,35 @@ int pick_nt(int rows) {
   return r16 > 256 ? 256 : r16;
 }
 
+// Launch as a programmatic dependent of the previous kernel in the stream.
+// max_stages bounds the ring (the per-head decode GEMMs keep all of K in
+// flight, the split-K projections four stages and two CTAs per SM).
 template <bool kAMnMajor>
 cudaError_t launch_head_gemm(const CUtensorMap &tmA, const CUtensorMap &tmA2,
-                             const CUtensorMap &tmB, GemmArgs g, int m_tiles, cudaStream_t st) {
-  g.stages = g.num_k_chunks < kMaxStages ? g.num_k_chunks : kMaxStages;
-  const size_t smem = 1024 + (size_t)g.stages * (kABytes + g.Nt * 128);
+                             const CUtensorMap &tmB, GemmArgs g, int m_tiles, cudaStream_t st,
+                             int max_stages = 4) {
+  const size_t stage_bytes = kABytes + (size_t)g.Nt * 128;
+  const int fit = (int)((200u << 10) / stage_bytes);  // leave room below 227 KB
+  int stages = g.num_k_chunks < max_stages ? g.num_k_chunks : max_stages;
+  if (stages > fit) stages = fit;
+  if (stages > kMaxStages) stages = kMaxStages;
+  g.stages = stages < 1 ? 1 : stages;
+  const size_t smem = 1024 + (size_t)g.stages * stage_bytes;
   auto kern = head_gemm_kernel<kAMnMajor>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
-  dim3 grid(m_tiles, g.H, (g.rows + g.Nt - 1) / g.Nt);
-  kern<<<grid, 128, smem, st>>>(tmA, tmA2, tmB, g);
-  return cudaGetLastError();
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(m_tiles, g.H, (g.rows + g.Nt - 1) / g.Nt);
+  cfg.blockDim = dim3(128, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = pdl;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tmA, tmA2, tmB, g);
 }
 
 }  // namespace
@@ -253,7 +289,7 @@ cudaError_t launch_absorb_tc(const void *q_nope, const void *W_UK, void *q_lat, 
   g.part = nullptr;
   g.m_ofs = 0;
   g.a_tiles = 1 << 30;
-  return launch_head_gemm<true>(tmA, tmA, tmB, g, d.d_c / kM, st);
+  return launch_head_gemm<true>(tmA, tmA, tmB, g, d.d_c / kM, st, kMaxStages);
 }
 
 cudaError_t launch_out_proj_tc(const void *o_lat, const void *W_UV, void *out, int rows,
@@ -281,7 +317,7 @@ cudaError_t launch_out_proj_tc(const void *o_lat, const void *W_UV, void *out, i
   g.part = nullptr;
   g.m_ofs = 0;
   g.a_tiles = 1 << 30;
-  return launch_head_gemm<false>(tmA, tmA, tmB, g, 1, st);
+  return launch_head_gemm<false>(tmA, tmA, tmB, g, 1, st, kMaxStages);
 }
 
 // ---- fused latent / RoPE-key projection into the paged cache ----

@@ -64,3 +64,28 @@ def test_whole_job_rate_counts_every_replica():
     assert bench.whole_job_rate(1e9, 1, 1.0) == pytest.approx(1e12)
     assert bench.whole_job_rate(1e9, 4, 2.0) == pytest.approx(2e12)
     assert bench.max_over_ranks([1, 2.5], 1) == [1.0, 2.5]
+
+
+CHILD = r"""
+import os, sys, torch, torch.distributed as dist
+dist.init_process_group("gloo")
+t = torch.tensor([float(os.environ["RANK"]) + 1.0])
+dist.all_reduce(t)
+assert os.environ["LOCAL_RANK"] == os.environ["RANK"]
+assert os.environ["MASTER_ADDR"] == "127.0.0.1"
+print("rank", os.environ["RANK"], "of", os.environ["WORLD_SIZE"], "sum", t.item(), flush=True)
+dist.destroy_process_group()
+"""
+
+
+def test_bench_starts_its_own_ranks(capfd):
+    """``bench.py --gpus N`` without torchrun starts N rank processes with the
+    torchrun environment and a local rendezvous; here two gloo children
+    rendezvous and all-reduce on the CPU."""
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+    rc = bench.spawn_ranks(2, [sys.executable, "-c", CHILD])
+    assert rc == 0
+    out = capfd.readouterr().out
+    assert "rank 0 of 2 sum 3.0" in out and "rank 1 of 2 sum 3.0" in out
