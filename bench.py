@@ -378,14 +378,14 @@ def run_ours(args, rank, world, device):
 OTHER_CONFIGS = ("lite", "mtp", "long")
 
 
-def measure_other_configs(mla, args, flush, stream, device):
+def measure_other_configs(mla, args, flush, stream, device, names=OTHER_CONFIGS):
     """``mla_decode`` alone on each of the other workloads, with its own
     inputs (the same seeded recipe as the parity tests), L2 flushed before
     every call: time, cache GB/s, TFLOP/s and the fraction of
     ``max(bytes / HBM, FLOPs / bf16 peak)``, the same roofline as the step's."""
     peaks, _ = load_peaks()
     out = {}
-    for name in OTHER_CONFIGS:
+    for name in names:
         if name == args.workload:
             continue
         inp, dev = setup_inputs(name, device)
@@ -712,6 +712,21 @@ def run_reference(args, rank):
     }
 
 
+def run_decode_only(args, device):
+    """``--decode-only``: ``mla_decode`` alone on the chosen workload (for
+    profiling one workload's decode kernel), same timing and roofline as the
+    ``configs`` record of the full run."""
+    import mla_latent_kv_74_b300 as mla
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+    res = measure_other_configs(mla, argparse.Namespace(workload=None, steps=args.steps),
+                                flush, stream, device, names=(args.workload,))
+    r = res[args.workload]
+    return {"metric": "mla_decode time, fraction of max(bytes/HBM, FLOPs/bf16 peak)",
+            "value": r["roofline_time_frac"], "unit": "fraction", "higher_is_better": True,
+            "dtype": "bf16", "data": "synthetic", "decode": r}
+
+
 def run_prefill_only(args, device):
     """``--prefill-only``: the prefill measurement alone (for profiling it)."""
     import mla_latent_kv_74_b300 as mla
@@ -769,6 +784,8 @@ def main():
                     help="seconds of oracle work per step of the reference arm")
     ap.add_argument("--prefill-only", action="store_true",
                     help="time only mla_prefill (four 4096-token prompts) and print its line")
+    ap.add_argument("--decode-only", action="store_true",
+                    help="time only mla_decode on --workload and print its line")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -783,6 +800,13 @@ def main():
         res = run_reference(args, rank)
         if res is not None:
             print(json.dumps(res), flush=True)
+        return
+
+    if args.decode_only:
+        if rank == 0:
+            device = torch.device("cuda", local_rank)
+            torch.cuda.set_device(device)
+            print(json.dumps(run_decode_only(args, device)), flush=True)
         return
 
     if args.prefill_only:

@@ -51,6 +51,11 @@
 // cut by a range boundary write fp32 partials (O/l and lse) that
 // combine_tc_kernel merges with log-sum-exp weights; whole items are written
 // directly.  The plan is computed on the device from seqlens (no host sync).
+// With several query slots per sequence the items are laid out slot by slot
+// and each slot gets its own equal share of the pairs, so pair j of every
+// slot walks the same sequences' pages at the same time: the slots after the
+// first find each page in L2 (or merge with its miss in flight) instead of
+// reading the cache from HBM again.
 //
 // Warp roles (352 threads per CTA): warp 0 TMA producer, warp 1 TMEM owner
 // and MMA issuer; S-CTA: warp 6 second QK^T issuer, warps 2-5 and 7-10 the
@@ -172,9 +177,12 @@ struct DecodeArgs {
   float scale_log2;
   __nv_bfloat16 *o_lat;
   float *lse;
-  float *o_part;    // [2 * kMaxPairs][128][512]
+  __nv_bfloat16 *o_part;  // [2 * kMaxPairs][128][512] (O / l of split pieces)
   float *lse_part;  // [2 * kMaxPairs][128]
-  int *plan;        // [0] = tiles per pair, [1..W+1] = prefix of tiles per item
+  // plan: [0] = number of slot groups G (1 or Hq), [1+g] = units per pair of
+  // group g, [1+Hq+u] = prefix of units per item in plan order u (u = slot *
+  // B + b for item b * Hq + slot), u = 0..W
+  int *plan;
   int *err;
 };
 
@@ -240,9 +248,19 @@ __device__ __forceinline__ bool wait_bar_warp(uint64_t *bar, uint32_t parity, vo
 // item with n > 0 tiles spans kItemCost + n units, the first kItemCost
 // standing for its start-up cost and holding no tile: unit u of the span is
 // tile u - kItemCost.
+// Item of plan position u.  With one query slot the plan follows the items;
+// with several (kSlotMajor) it lists every sequence's slot 0, then every
+// sequence's slot 1, and so on.
+template <bool kSlotMajor>
+__device__ __forceinline__ int item_at(const DecodeArgs &a, int u) {
+  return kSlotMajor ? (u % a.B) * a.Hq + u / a.B : u;
+}
+
+template <bool kSlotMajor>
 struct SegIter {
   const DecodeArgs *a;
-  int W, t_begin, t_end, w, s;
+  int W, t_begin, t_end, w, s;  // w: item (walked in plan order)
+  // w0: the item at the start of the range (W if none), s0: its first unit
   __device__ void init(const DecodeArgs *args, int W_, int tb, int te, int w0, int s0) {
     a = args;
     W = W_;
@@ -258,7 +276,18 @@ struct SegIter {
       const int n = visible_len(*a, w, &bad);
       const int nt = (n + kTile - 1) / kTile;
       const int st = s, e = nt > 0 ? s + kItemCost + nt : s;
-      const int cur = w++;
+      const int cur = w;
+      if (kSlotMajor) {
+        // the same slot of the next sequence; past the last sequence, the
+        // next slot's first sequence (or the end after the last slot)
+        w += a->Hq;
+        if (w >= W) {
+          w -= W - 1;
+          if (w >= a->Hq) w = W;
+        }
+      } else {
+        ++w;
+      }
       s = e;
       if (e <= st || e <= t_begin) continue;
       const int g0 = st > t_begin ? st : t_begin;
@@ -304,6 +333,7 @@ __device__ __forceinline__ void signal_abort(Misc *misc, uint32_t peer) {
   ptx::st_cluster_s32(ptx::map_to_rank(&misc->abort, peer), 1);
 }
 
+template <bool kSlotMajor>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tm_cache,
                      const __grid_constant__ CUtensorMap tm_cache_v,
@@ -383,12 +413,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // tiles per item -> scan (scratch in the ring) -> this pair's range
     int *pre = reinterpret_cast<int *>(smem + kOffRing);
     bool any_bad = false;
-    for (int w = threadIdx.x; w < W; w += blockDim.x) {
+    for (int u = threadIdx.x; u < W; u += blockDim.x) {
       bool bad = false;
-      const int n = visible_len(a, w, &bad);
+      const int n = visible_len(a, item_at<kSlotMajor>(a, u), &bad);
       any_bad |= bad;
       const int nt = (n + kTile - 1) / kTile;
-      pre[w + 1] = nt > 0 ? nt + kItemCost : 0;
+      pre[u + 1] = nt > 0 ? nt + kItemCost : 0;
     }
     if (any_bad && pair == 0) set_device_error(a.err, kDevBounds);
     __syncthreads();
@@ -397,7 +427,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int base = 0; base < W; base += 32) {
         const int idx = base + lane;
         int v = idx < W ? pre[idx + 1] : 0;
-#pragma unroll
+  #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
           const int u = __shfl_up_sync(0xffffffffu, v, off);
           if (lane >= off) v += u;
@@ -408,26 +438,65 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (lane == 0) pre[0] = 0;
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-      const int t_total = pre[W];
-      const int per = (t_total + a.npairs - 1) / a.npairs;
-      const int tb = min(t_total, pair * per);
-      const int te = min(t_total, tb + per);
-      int lo = 0, hi = W;  // first item whose tile range ends after tb
-      while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (pre[mid + 1] <= tb) lo = mid + 1;
-        else hi = mid;
+    if constexpr (kSlotMajor) {
+      // slot groups: each query slot's items over its own share of the pairs
+#ifdef MLA_FORCE_ONE_GROUP
+      const int ngroups = 1;
+#else
+      const int ngroups = a.npairs >= a.Hq ? a.Hq : 1;
+#endif
+      const int pairs_per_group = a.npairs / ngroups;
+      if (threadIdx.x == 0) {
+        const int t_total = pre[W];
+        const int g = pair / pairs_per_group, j = pair % pairs_per_group;
+        const int g0 = g < ngroups ? pre[g * (W / ngroups)] : t_total;
+        const int g1 = g < ngroups ? pre[(g + 1) * (W / ngroups)] : t_total;
+        const int per = (g1 - g0 + pairs_per_group - 1) / pairs_per_group;
+        const int tb = min(g1, g0 + j * per);
+        const int te = min(g1, tb + per);
+        int lo = 0, hi = W;  // first plan position whose tile range ends after tb
+        while (lo < hi) {
+          const int mid = (lo + hi) >> 1;
+          if (pre[mid + 1] <= tb) lo = mid + 1;
+          else hi = mid;
+        }
+        misc->t_begin = tb;
+        misc->t_end = te;
+        misc->w0 = lo < W ? item_at<true>(a, lo) : W;  // the SegIter walks items
+        misc->s0 = lo < W ? pre[lo] : t_total;
+        misc->t_total = t_total;
+        if (pair == 0) {
+          a.plan[0] = ngroups;
+          for (int gg = 0; gg < ngroups; ++gg) {
+            const int span = pre[(gg + 1) * (W / ngroups)] - pre[gg * (W / ngroups)];
+            a.plan[1 + gg] = (span + pairs_per_group - 1) / pairs_per_group;
+          }
+        }
       }
-      misc->t_begin = tb;
-      misc->t_end = te;
-      misc->w0 = lo;
-      misc->s0 = lo < W ? pre[lo] : t_total;
-      misc->t_total = t_total;
-      if (pair == 0) a.plan[0] = per;
+      if (pair == 0)  // the plan of the combine kernel
+        for (int u = threadIdx.x; u <= W; u += blockDim.x) a.plan[1 + a.Hq + u] = pre[u];
+    } else {
+      if (threadIdx.x == 0) {
+        const int t_total = pre[W];
+        const int per = (t_total + a.npairs - 1) / a.npairs;
+        const int tb = min(t_total, pair * per);
+        const int te = min(t_total, tb + per);
+        int lo = 0, hi = W;  // first item whose tile range ends after tb
+        while (lo < hi) {
+          const int mid = (lo + hi) >> 1;
+          if (pre[mid + 1] <= tb) lo = mid + 1;
+          else hi = mid;
+        }
+        misc->t_begin = tb;
+        misc->t_end = te;
+        misc->w0 = lo;
+        misc->s0 = lo < W ? pre[lo] : t_total;
+        misc->t_total = t_total;
+        if (pair == 0) a.plan[0] = per;
+      }
+      if (pair == 0)  // the plan of the combine kernel
+        for (int w = threadIdx.x; w <= W; w += blockDim.x) a.plan[1 + w] = pre[w];
     }
-    if (pair == 0)  // the plan of the combine kernel
-      for (int w = threadIdx.x; w <= W; w += blockDim.x) a.plan[1 + w] = pre[w];
     __syncthreads();  // the scratch is the ring: read before the first load
   }
   ptx::tc_fence_before();
@@ -455,7 +524,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) set_device_error(a.err, kDevTimeout);
   } else if (warp == 0) {
     // ===================== TMA producer (each CTA its own ring) =====================
-    SegIter it;
+    SegIter<kSlotMajor> it;
     it.init(&a, W, t_begin, t_end, w0, s0);
     int item, lt0, lt1, n_vis, g = 0;
     bool whole, failed = false;
@@ -516,7 +585,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int mine = warp == 1 ? 0 : 1;
       const uint32_t idesc = ptx::idesc_bf16(128, kTile, false, false);
       const uint64_t ring_desc = ptx::smem_desc(ptx::smem_u32(smem + kOffRing), 16, 1024, ptx::kSw128);
-      SegIter it;
+      SegIter<kSlotMajor> it;
       it.init(&a, W, t_begin, t_end, w0, s0);
       int item, lt0, lt1, n_vis, seg = 0, g = 0, r = 0;
       bool whole, failed = false;
@@ -567,7 +636,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint64_t ring_desc =
           ptx::smem_desc(ptx::smem_u32(smem + kOffRing), 4 * 2048, 1024, ptx::kSw128);
       const uint8_t *aux = smem + kOffAux;
-      SegIter it;
+      SegIter<kSlotMajor> it;
       it.init(&a, W, t_begin, t_end, w0, s0);
       int item, lt0, lt1, n_vis, seg = 0, g = 0, nev = 0, npv = 0;
       bool whole, failed = false;
@@ -659,7 +728,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t rStatsFull = ptx::map_to_rank(&bars->stats_full, kRankV);
     const float c = a.scale_log2;
     (void)gtid;
-    SegIter it;
+    SegIter<kSlotMajor> it;
     it.init(&a, W, t_begin, t_end, w0, s0);
     int item, lt0, lt1, n_vis, seg = 0, g = 0, r_pos = 0;
     bool whole, failed = false;
@@ -920,7 +989,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = (uint32_t)(32 * wq) << 16;
     const uint8_t *aux = smem + kOffAux;
     const float *stats = reinterpret_cast<const float *>(smem + kOffStats);
-    SegIter it;
+    SegIter<kSlotMajor> it;
     it.init(&a, W, t_begin, t_end, w0, s0);
     int item, lt0, lt1, n_vis, seg = 0, nev = 0;
     bool whole, failed = false;
@@ -975,11 +1044,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // pieces to global memory.
       uint8_t *stg = smem + kOffP + pb * kPBytes + wq * 4096;  // 32 rows x 128 B
       const int slot_idx = 2 * pair + ((lt0 == 0) ? 1 : 0);    // partial slot
-      // whole items: bf16 rows of o_lat; partial items: fp32 rows of o_part
+      // whole items: rows of o_lat; split pieces: rows of o_part (both bf16)
       uint8_t *dst_base = whole
           ? reinterpret_cast<uint8_t *>(a.o_lat + ((size_t)item * a.H + 32 * wq) * kDc)
           : reinterpret_cast<uint8_t *>(a.o_part + ((size_t)slot_idx * 128 + 32 * wq) * kDc);
-      const size_t dst_row_bytes = whole ? kDc * 2 : kDc * 4;
+      const size_t dst_row_bytes = kDc * 2;
       const int rows_here = whole ? min(32, a.H - 32 * wq) : 32;  // rows of this item
       // one staged 128-byte piece per row: thread = row in, lane = 16 B out
       auto flush_piece = [&](const uint32_t (&pk)[32], size_t byte_off) {
@@ -1014,13 +1083,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) pk[i] = ptx::pack_bf16x2(v[2 * i] * inv_l, v[2 * i + 1] * inv_l);
           flush_piece(pk, (size_t)q * 128);
-        } else {  // 64 fp32 = two 128-byte pieces
+        } else {  // a split piece: the same bf16 piece into o_part (two branches
+                  // on purpose: one branch costs the main loops registers)
 #pragma unroll
-          for (int hp = 0; hp < 2; ++hp) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) pk[i] = __float_as_uint(v[32 * hp + i] * inv_l);
-            flush_piece(pk, (size_t)q * 256 + hp * 128);
-          }
+          for (int i = 0; i < 32; ++i) pk[i] = ptx::pack_bf16x2(v[2 * i] * inv_l, v[2 * i + 1] * inv_l);
+          flush_piece(pk, (size_t)q * 128);
         }
       }
       if (whole) {
@@ -1061,6 +1128,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 // piece row is read as 2 KB of coalesced loads.  Rows of items written
 // directly by their pair return at once.
 constexpr int kCombineRows = 8;
+
+// Columns 16 lane .. 16 lane + 15 of one bf16 piece row, as fp32.
+__device__ __forceinline__ void load_piece16(const __nv_bfloat16 *row, int lane, float (&v)[16]) {
+  const uint4 *src = reinterpret_cast<const uint4 *>(row) + lane * 2;
+  const uint4 x0 = src[0], x1 = src[1];
+  const uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    v[2 * i] = __uint_as_float(w[i] << 16);
+    v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+template <bool kSlotMajor>
 __global__ void __launch_bounds__(32 * kCombineRows) combine_tc_kernel(DecodeArgs a) {
   // launched early, behind the decode grid: its pieces are complete and
   // visible only after this wait; the next kernel may launch after it
@@ -1080,29 +1160,40 @@ __global__ void __launch_bounds__(32 * kCombineRows) combine_tc_kernel(DecodeArg
   const int W = a.B * a.Hq;
   if (rowg >= (long)W * a.H) return;
   const int w = (int)(rowg / a.H), h = (int)(rowg % a.H);
-  const int per = a.plan[0];
-  const int s = a.plan[1 + w], e = a.plan[2 + w];
-  if (e <= s || per <= 0) return;
-  // the item's tiles are units s + kItemCost .. e - 1 of the plan
-  const int f = s + kItemCost;
+  int per, f, e, grp_pair0;  // the item's tiles are units f .. e - 1 of its group
+  if constexpr (kSlotMajor) {
+    // the item's plan position and slot group (as in decode_tc_kernel)
+    const int u = (w % a.Hq) * a.B + w / a.Hq;
+    const int ngroups = a.plan[0];
+    const int grp = ngroups > 1 ? w % a.Hq : 0;
+    const int *pre = a.plan + 1 + a.Hq;
+    const int base = pre[grp * (W / ngroups)];
+    per = a.plan[1 + grp];
+    const int s = pre[u] - base;
+    e = pre[u + 1] - base;
+    if (e <= s) return;
+    f = s + kItemCost;
+    grp_pair0 = grp * (a.npairs / ngroups);
+  } else {
+    per = a.plan[0];
+    const int s = a.plan[1 + w];
+    e = a.plan[2 + w];
+    if (e <= s) return;
+    f = s + kItemCost;
+    grp_pair0 = 0;
+  }
+  if (per <= 0) return;
   const int p0 = f / per, p1 = (e - 1) / per;
   if (p0 == p1) return;  // written directly by its pair
-  auto slot_of = [&](int p) { return 2 * p + ((f < p * per) ? 0 : 1); };
+  auto slot_of = [&](int p) { return 2 * (grp_pair0 + p) + ((f < p * per) ? 0 : 1); };
   __nv_bfloat16 *dst = a.o_lat + (size_t)rowg * kDc;
   if (p1 == p0 + 1) {
     // two pieces (an item cut once): every load in flight at once
     const int s0 = slot_of(p0), s1 = slot_of(p1);
     const float l0 = a.lse_part[(size_t)s0 * 128 + h], l1 = a.lse_part[(size_t)s1 * 128 + h];
-    const float4 *src0 =
-        reinterpret_cast<const float4 *>(a.o_part + ((size_t)s0 * 128 + h) * kDc) + lane * 4;
-    const float4 *src1 =
-        reinterpret_cast<const float4 *>(a.o_part + ((size_t)s1 * 128 + h) * kDc) + lane * 4;
-    float4 v0[4], v1[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      v0[q] = src0[q];
-      v1[q] = src1[q];
-    }
+    float v0[16], v1[16];
+    load_piece16(a.o_part + ((size_t)s0 * 128 + h) * kDc, lane, v0);
+    load_piece16(a.o_part + ((size_t)s1 * 128 + h) * kDc, lane, v1);
     const float mx2 = fmaxf(l0, l1);
     if (isnan(l0) || isnan(l1) || mx2 == -INFINITY) {
       reinterpret_cast<uint4 *>(dst)[lane] = make_uint4(0, 0, 0, 0);
@@ -1114,11 +1205,9 @@ __global__ void __launch_bounds__(32 * kCombineRows) combine_tc_kernel(DecodeArg
     const float inv2 = 1.f / (w0 + w1), a0 = w0 * inv2, a1 = w1 * inv2;
     uint32_t pk[8];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      pk[2 * q] = ptx::pack_bf16x2(fmaf(a1, v1[q].x, a0 * v0[q].x), fmaf(a1, v1[q].y, a0 * v0[q].y));
-      pk[2 * q + 1] =
-          ptx::pack_bf16x2(fmaf(a1, v1[q].z, a0 * v0[q].z), fmaf(a1, v1[q].w, a0 * v0[q].w));
-    }
+    for (int i = 0; i < 8; ++i)
+      pk[i] = ptx::pack_bf16x2(fmaf(a1, v1[2 * i], a0 * v0[2 * i]),
+                               fmaf(a1, v1[2 * i + 1], a0 * v0[2 * i + 1]));
     uint4 *d4 = reinterpret_cast<uint4 *>(dst) + lane * 2;
     d4[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
     d4[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
@@ -1157,17 +1246,10 @@ __global__ void __launch_bounds__(32 * kCombineRows) combine_tc_kernel(DecodeArg
     const int n = min(32, p1 - base + 1);
     for (int j = 0; j < n; ++j) {
       const float wgt = __shfl_sync(0xffffffffu, wl, j);
-      const float4 *src =
-          reinterpret_cast<const float4 *>(a.o_part + ((size_t)slot_of(base + j) * 128 + h) * kDc) +
-          lane * 4;
+      float v[16];
+      load_piece16(a.o_part + ((size_t)slot_of(base + j) * 128 + h) * kDc, lane, v);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float4 v = src[q];
-        acc[4 * q] = fmaf(wgt, v.x, acc[4 * q]);
-        acc[4 * q + 1] = fmaf(wgt, v.y, acc[4 * q + 1]);
-        acc[4 * q + 2] = fmaf(wgt, v.z, acc[4 * q + 2]);
-        acc[4 * q + 3] = fmaf(wgt, v.w, acc[4 * q + 3]);
-      }
+      for (int i = 0; i < 16; ++i) acc[i] = fmaf(wgt, v[i], acc[i]);
     }
   }
   uint32_t pk[8];
@@ -1179,9 +1261,13 @@ __global__ void __launch_bounds__(32 * kCombineRows) combine_tc_kernel(DecodeArg
   if (lane == 0) a.lse[rowg] = mx + logf(sum);
 }
 
-size_t part_bytes() { return align_up((size_t)2 * kMaxPairs * 128 * kDc * sizeof(float), 256); }
+size_t part_bytes() {
+  return align_up((size_t)2 * kMaxPairs * 128 * kDc * sizeof(__nv_bfloat16), 256);
+}
 size_t lse_part_bytes() { return align_up((size_t)2 * kMaxPairs * 128 * sizeof(float), 256); }
-size_t plan_bytes(int B, int Hq) { return align_up(((size_t)B * Hq + 2) * sizeof(int), 256); }
+size_t plan_bytes(int B, int Hq) {
+  return align_up(((size_t)B * Hq + 2 + Hq) * sizeof(int), 256);
+}
 
 // Test hook: at most this many CTA pairs take part in the split plan (0:
 // no limit).  Set through mla_debug_set_decode_pairs.
@@ -1206,7 +1292,8 @@ int pairs_on_device() {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, decode_tc_kernel, &cfg) != cudaSuccess || n <= 0) {
+  if (cudaOccupancyMaxActiveClusters(&n, decode_tc_kernel<false>, &cfg) != cudaSuccess ||
+      n <= 0) {
     cudaGetLastError();
     n = kMaxPairs;
   }
@@ -1255,7 +1342,7 @@ cudaError_t launch_decode_tc(const void *q_lat, const void *q_rope, const void *
                              const mla_dims &d, float scale, void *o_lat, float *lse,
                              void *workspace, cudaStream_t st) {
   char *ws = static_cast<char *>(workspace);
-  float *o_part = reinterpret_cast<float *>(ws + kWsHeader);
+  __nv_bfloat16 *o_part = reinterpret_cast<__nv_bfloat16 *>(ws + kWsHeader);
   const uint64_t rows = (uint64_t)B * Hq * d.H;
   // The cache and q_lat as [column block of 64][row][64]: one copy moves a
   // whole stage, box k of it (columns 64k..64k+63) 8 KB after box k-1, each
@@ -1271,8 +1358,12 @@ cudaError_t launch_decode_tc(const void *q_lat, const void *q_rope, const void *
       !make_tmap_2d_bf16(&tm_qrope, q_rope, kDr, rows, kDr * 2, 64, 64,
                          CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+  // several query slots: the slot-major plan (each slot over its own share
+  // of the pairs); one slot: items in order
+  const bool slot_major = Hq > 1;
+  auto decode_kernel = slot_major ? decode_tc_kernel<true> : decode_tc_kernel<false>;
+  auto combine_kernel = slot_major ? combine_tc_kernel<true> : combine_tc_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)kSmemBytes);
   if (e != cudaSuccess) return e;
   const int npairs = pairs_for_device();
@@ -1314,13 +1405,13 @@ cudaError_t launch_decode_tc(const void *q_lat, const void *q_rope, const void *
   cfg.stream = st;
   cfg.attrs = pdl;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, decode_tc_kernel, tm_cache, tm_cache_v, tm_qlat, tm_qrope, a);
+  e = cudaLaunchKernelEx(&cfg, decode_kernel, tm_cache, tm_cache_v, tm_qlat, tm_qrope, a);
   if (e != cudaSuccess) return e;
   const long rows_total = (long)B * Hq * d.H;
   cfg.gridDim = dim3((unsigned)((rows_total + kCombineRows - 1) / kCombineRows), 1, 1);
   cfg.blockDim = dim3(32 * kCombineRows, 1, 1);
   cfg.dynamicSmemBytes = 0;
-  return cudaLaunchKernelEx(&cfg, combine_tc_kernel, a);
+  return cudaLaunchKernelEx(&cfg, combine_kernel, a);
 }
 
 }  // namespace mla

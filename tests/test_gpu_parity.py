@@ -176,24 +176,32 @@ def test_block_table_permutation_invariance(mla):
 
 
 def _pieces(seqlens, Hq, npairs, item_cost=6, tile=64):
-    """How many split pieces each (sequence, slot) item is cut into when its
-    tiles, each item preceded by ``item_cost`` start-up units, are laid end
-    to end and cut into ``npairs`` equal ranges (the tensor-core decode's
-    plan); used to show which piece counts a sweep covers."""
-    units, spans = 0, []
-    for n_seq in seqlens:
-        for i in range(Hq):
-            nt = -(-max(0, n_seq - Hq + i + 1) // tile)
-            if nt:
-                spans.append((units + item_cost, units + item_cost + nt))
-                units += item_cost + nt
-    per = -(-units // npairs)
-    return [(e - 1) // per - s // per + 1 for s, e in spans]
+    """How many split pieces each (sequence, slot) item is cut into by the
+    tensor-core decode's plan: items laid out slot by slot, each preceded by
+    ``item_cost`` start-up units; with several slots (and at least as many
+    pairs as slots) each slot's items are cut into equal ranges over its own
+    share of the pairs, else all items over all pairs.  Used to show which
+    piece counts a sweep covers."""
+    groups = Hq if (Hq > 1 and npairs >= Hq) else 1
+    per_group = npairs // groups
+    slots = [list(range(Hq))] if groups == 1 else [[i] for i in range(Hq)]
+    pieces = []
+    for slot_set in slots:
+        units, spans = 0, []
+        for i in slot_set:
+            for n_seq in seqlens:
+                nt = -(-max(0, n_seq - Hq + i + 1) // tile)
+                if nt:
+                    spans.append((units + item_cost, units + item_cost + nt))
+                    units += item_cost + nt
+        per = -(-units // per_group)
+        pieces += [(e - 1) // per - s // per + 1 for s, e in spans]
+    return pieces
 
 
 SPLIT_CASES = {
     "hq1": ([4000, 300, 64, 1, 900, 2500], 1),
-    "hq2": ([4500, 70, 5, 1400], 2),
+    "hq2": ([5000, 70, 5, 130], 2),
 }
 
 
