@@ -378,7 +378,7 @@ def run_ours(args, rank, world, device):
 OTHER_CONFIGS = ("lite", "mtp", "long")
 
 
-def measure_other_configs(mla, args, flush, stream, device, names=OTHER_CONFIGS):
+def measure_other_configs(mla, args, flush, stream, device, names=OTHER_CONFIGS, batch=None):
     """``mla_decode`` alone on each of the other workloads, with its own
     inputs (the same seeded recipe as the parity tests), L2 flushed before
     every call: time, cache GB/s, TFLOP/s and the fraction of
@@ -388,7 +388,7 @@ def measure_other_configs(mla, args, flush, stream, device, names=OTHER_CONFIGS)
     for name in names:
         if name == args.workload:
             continue
-        inp, dev = setup_inputs(name, device)
+        inp, dev = setup_inputs(name, device, batch)
         w = inp["workload"]
         seqlens = inp["seqlens"].numpy()
         max_seqlen = int(seqlens.max())
@@ -412,7 +412,7 @@ def measure_other_configs(mla, args, flush, stream, device, names=OTHER_CONFIGS)
         flops, nbytes = decode_work(w, seqlens)
         t_mem, t_tc = nbytes / (peaks["hbm_gbs"] * 1e9), flops / (peaks["bf16_tflops"] * 1e12)
         out[name] = {
-            "workload": synth.DESCRIPTIONS[name],
+            "workload": synth.DESCRIPTIONS[name] + ("" if batch is None else f" (batch {w.B})"),
             "ms": round(ms, 5),
             "cache_gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
             "tflops": round(flops / (ms * 1e-3) / 1e12, 2),
@@ -720,7 +720,7 @@ def run_decode_only(args, device):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream(device)
     res = measure_other_configs(mla, argparse.Namespace(workload=None, steps=args.steps),
-                                flush, stream, device, names=(args.workload,))
+                                flush, stream, device, names=(args.workload,), batch=args.batch)
     r = res[args.workload]
     return {"metric": "mla_decode time, fraction of max(bytes/HBM, FLOPs/bf16 peak)",
             "value": r["roofline_time_frac"], "unit": "fraction", "higher_is_better": True,
