@@ -264,60 +264,183 @@ int read_and_clear_gemm_error() {
   return v;
 }
 
+// ---- absorb and out-proj: one CTA per (head, row tile), whole operands ----
+//
+// Each per-head GEMM of the decode step is small (a 128 x 512 weight, at most
+// a few hundred query rows), so a CTA takes a whole head: the weight arrives
+// in ONE 3-D TMA copy (8 column blocks of 64, 128 KB) and the head's query
+// rows in one more.  One SM completes only about two copies per microsecond,
+// so the copy count, not the bytes, set the time of the chunked version.
+//   absorb:   D[c][r] = W_UK[h][a][c] q_nope[r][h][a]: four M = 128 tiles of
+//             c, N = query rows, K = a (d_h = 128); A read MN-major.
+//   out_proj: D[a][r] = W_UV[h][a][c] o_lat[r][h][c]: M = a (128), N = rows,
+//             K = c (d_c = 512); both operands K-major.
+// The weight copy is issued before waiting for the previous kernel (no kernel
+// of this library writes weights); the rows are read after the wait.
+
+namespace {
+
+constexpr uint32_t kWholeA = 128 * 512 * 2;  // one head's weight, 128 KB
+
+template <bool kAbsorb>
+__global__ void __launch_bounds__(128, 1)
+    head_whole_kernel(const __grid_constant__ CUtensorMap tmA,
+                      const __grid_constant__ CUtensorMap tmB, __nv_bfloat16 *out, int rows,
+                      int Nt, int H) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t *sA = smem, *sB = smem + kWholeA;
+  __shared__ uint64_t full, done;
+  __shared__ uint32_t tmem_base;
+  __shared__ int fail;
+  constexpr int kMTiles = kAbsorb ? 4 : 1;       // M tiles of 128
+  constexpr int kBBlocks = kAbsorb ? 2 : 8;      // 64-wide K blocks of B
+  constexpr int kKSteps = kAbsorb ? 8 : 32;      // K-steps of 16
+  const int warp = threadIdx.x >> 5;
+  const int h = blockIdx.x, n0 = blockIdx.y * Nt;
+  const uint32_t b_bytes = (uint32_t)kBBlocks * Nt * 128;
+  const int cols = kMTiles * Nt;  // TMEM: a power of two >= 32
+  const uint32_t ncols = cols <= 32 ? 32 : cols <= 64 ? 64 : cols <= 128 ? 128 : cols <= 256 ? 256 : 512;
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(&full, 1);
+    ptx::mbar_init(&done, 1);
+    ptx::fence_mbar_init();
+    fail = 0;
+  }
+  if (warp == 2) ptx::tmem_alloc(&tmem_base, ncols);
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = tmem_base;
+
+  if (warp == 0 && ptx::elect_lane0()) {
+    ptx::mbar_arrive_expect_tx(&full, kWholeA + b_bytes);
+    // the weight: [64-column block][128 rows][64], one copy
+    ptx::tma_load_3d(sA, &tmA, &full, 0, h * 128, 0);
+    ptx::grid_dependency_wait();  // the rows may come from the previous kernel
+    ptx::launch_dependents();
+    ptx::tma_load_3d(sB, &tmB, &full, 0, n0, h * kBBlocks);
+  } else if (warp == 1 && ptx::elect_lane0()) {
+    const uint32_t idesc = ptx::idesc_bf16(128, Nt, kAbsorb, false);
+    if (!ptx::mbar_wait(&full, 0, &fail)) {
+      atomicExch(&fail, 1);
+    } else {
+      ptx::tc_fence_after();
+      const uint32_t a_addr = ptx::smem_u32(sA), b_addr = ptx::smem_u32(sB);
+#pragma unroll
+      for (int m = 0; m < kMTiles; ++m) {
+#pragma unroll
+        for (int kk = 0; kk < kKSteps; ++kk) {
+          // A: absorb MN-major (c blocks 2m, 2m+1 of 128 a-rows, 16 KB apart;
+          // 16 a-rows per K-step); out-proj K-major (K-step kk in block kk/4)
+          const uint64_t adesc =
+              kAbsorb ? ptx::smem_desc(a_addr + 2 * m * 16384 + kk * 2048, 16384, 1024, ptx::kSw128)
+                      : ptx::smem_desc(a_addr + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024,
+                                       ptx::kSw128);
+          const uint64_t bdesc = ptx::smem_desc(b_addr + (kk >> 2) * (Nt * 128) + (kk & 3) * 32,
+                                                16, 1024, ptx::kSw128);
+          ptx::mma_bf16(tmem + m * Nt, adesc, bdesc, idesc, kk != 0);
+        }
+      }
+    }
+    ptx::mma_commit(&done);
+  }
+  __syncwarp();
+
+  // ---- epilogue: TMEM -> bf16 global, thread = output column (c or a) ----
+  const bool ok = ptx::mbar_wait(&done, 0);
+  ptx::tc_fence_after();
+  if (!ok || fail) atomicExch(&fail, 1);
+  if (ok && !fail) {
+    const int width = kAbsorb ? 512 : 128;
+    const size_t row_stride = (size_t)H * width;
+    for (int m = 0; m < kMTiles; ++m) {
+      __nv_bfloat16 *dst = out + (size_t)h * width + m * 128 + warp * 32 + (threadIdx.x & 31);
+      for (int c0 = 0; c0 < Nt; c0 += 16) {
+        float v[16];
+        ptx::tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + m * Nt + c0, v);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int n = n0 + c0 + i;
+          if (n < rows) dst[(size_t)n * row_stride] = __float2bfloat16_rn(v[i]);
+        }
+      }
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 2) ptx::tmem_dealloc(tmem, ncols);
+  if (threadIdx.x == 0 && fail) atomicCAS(&g_gemm_error, 0, kDevTimeout);
+}
+
+template <bool kAbsorb>
+cudaError_t launch_head_whole(const CUtensorMap &tmA, const CUtensorMap &tmB, void *out,
+                              int rows, int Nt, int H, cudaStream_t st) {
+  const int kBBlocks = kAbsorb ? 2 : 8;
+  const size_t smem = 1024 + kWholeA + (size_t)kBBlocks * Nt * 128;
+  auto kern = head_whole_kernel<kAbsorb>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(H, (rows + Nt - 1) / Nt, 1);
+  cfg.blockDim = dim3(128, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = pdl;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, static_cast<__nv_bfloat16 *>(out), rows, Nt,
+                            H);
+}
+
+// Query rows per CTA: a multiple of 16, at most `cap` (TMEM columns of the
+// absorb's four accumulators, shared memory of the out-proj's rows).
+int pick_rows_tile(int rows, int cap) {
+  const int r16 = (rows + 15) / 16 * 16;
+  return r16 > cap ? cap : r16;
+}
+
+}  // namespace
+
 cudaError_t launch_absorb_tc(const void *q_nope, const void *W_UK, void *q_lat, int rows,
                              const mla_dims &d, cudaStream_t st) {
   CUtensorMap tmA, tmB;
-  const int Nt = pick_nt(rows);
-  // W_UK as [H*d_h rows][d_c cols]; boxes of 64 c x 64 a.
-  if (!make_tmap_2d_bf16(&tmA, W_UK, d.d_c, (uint64_t)d.H * d.d_h, (uint64_t)d.d_c * 2, 64, 64,
-                         CU_TENSOR_MAP_SWIZZLE_128B))
+  const int Nt = pick_rows_tile(rows, 128);
+  // W_UK [H*d_h][d_c] as [column block of 64][row][64]: one box per head,
+  // 8 blocks x 128 rows
+  if (!make_tmap_3d(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W_UK, 64, (uint64_t)d.H * d.d_h,
+                    d.d_c / 64, (uint64_t)d.d_c * 2, 128, 64, 128, d.d_c / 64,
+                    CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  // q_nope as [rows][H*d_h]; boxes of 64 a x Nt rows.
-  if (!make_tmap_2d_bf16(&tmB, q_nope, (uint64_t)d.H * d.d_h, rows, (uint64_t)d.H * d.d_h * 2,
-                         64, Nt, CU_TENSOR_MAP_SWIZZLE_128B))
+  // q_nope [rows][H*d_h] as [block of 64][row][64]: two blocks of one head
+  if (!make_tmap_3d(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, q_nope, 64, rows,
+                    (uint64_t)d.H * d.d_h / 64, (uint64_t)d.H * d.d_h * 2, 128, 64, Nt, 2,
+                    CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  GemmArgs g;
-  g.num_k_chunks = d.d_h / kKChunk;
-  g.rows = rows;
-  g.Nt = Nt;
-  g.H = d.H;
-  g.M_total = d.d_c;
-  g.a_rows_per_head = d.d_h;
-  g.a_cols_per_head = 0;
-  g.b_cols_per_head = d.d_h;
-  g.out = static_cast<__nv_bfloat16 *>(q_lat);
-  g.part = nullptr;
-  g.m_ofs = 0;
-  g.a_tiles = 1 << 30;
-  return launch_head_gemm<true>(tmA, tmA, tmB, g, d.d_c / kM, st, kMaxStages);
+  return launch_head_whole<true>(tmA, tmB, q_lat, rows, Nt, d.H, st);
 }
 
 cudaError_t launch_out_proj_tc(const void *o_lat, const void *W_UV, void *out, int rows,
                                const mla_dims &d, cudaStream_t st) {
   CUtensorMap tmA, tmB;
-  const int Nt = pick_nt(rows);
-  // W_UV as [H*d_h rows][d_c cols]; boxes of 64 c x 128 a.
-  if (!make_tmap_2d_bf16(&tmA, W_UV, d.d_c, (uint64_t)d.H * d.d_h, (uint64_t)d.d_c * 2, 64, 128,
-                         CU_TENSOR_MAP_SWIZZLE_128B))
+  const int Nt = pick_rows_tile(rows, 64);
+  // W_UV [H*d_h][d_c] as [column block of 64][row][64]: one box per head
+  if (!make_tmap_3d(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W_UV, 64, (uint64_t)d.H * d.d_h,
+                    d.d_c / 64, (uint64_t)d.d_c * 2, 128, 64, 128, d.d_c / 64,
+                    CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  // o_lat as [rows][H*d_c]; boxes of 64 c x Nt rows.
-  if (!make_tmap_2d_bf16(&tmB, o_lat, (uint64_t)d.H * d.d_c, rows, (uint64_t)d.H * d.d_c * 2,
-                         64, Nt, CU_TENSOR_MAP_SWIZZLE_128B))
+  // o_lat [rows][H*d_c] as [block of 64][row][64]: eight blocks of one head
+  if (!make_tmap_3d(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, o_lat, 64, rows,
+                    (uint64_t)d.H * d.d_c / 64, (uint64_t)d.H * d.d_c * 2, 128, 64, Nt,
+                    d.d_c / 64, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  GemmArgs g;
-  g.num_k_chunks = d.d_c / kKChunk;
-  g.rows = rows;
-  g.Nt = Nt;
-  g.H = d.H;
-  g.M_total = d.d_h;
-  g.a_rows_per_head = d.d_h;
-  g.a_cols_per_head = 0;
-  g.b_cols_per_head = d.d_c;
-  g.out = static_cast<__nv_bfloat16 *>(out);
-  g.part = nullptr;
-  g.m_ofs = 0;
-  g.a_tiles = 1 << 30;
-  return launch_head_gemm<false>(tmA, tmA, tmB, g, 1, st, kMaxStages);
+  return launch_head_whole<false>(tmA, tmB, out, rows, Nt, d.H, st);
 }
 
 // ---- fused latent / RoPE-key projection into the paged cache ----
