@@ -134,8 +134,8 @@ struct Bars {
   // S: per tile g, barrier g % 6 (stage g % 3, issuer and softmax group
   // g % 2), so each barrier has one waiter that never falls a phase behind
   uint64_t sfull[6];                       // S: tile data landed
-  // S: partial scores of tile g from issuer h ready / read: index 2*(g%6)+h
-  uint64_t s_full[12], s_free[12];
+  // S: scores of tile g (TMEM buffer g % 3) ready / read: index g % 6
+  uint64_t s_full[6], s_free[6];
   uint64_t q_full, q_free;                 // S: query in TMEM / QK^T of a segment done
   uint64_t qfull[2];                       // S: query rows 64h..64h+63 landed in the ring
   uint64_t m_ready[2];                     // S: group i published its tile's maximum
@@ -189,13 +189,13 @@ struct DecodeArgs {
 #ifdef MLA_TRACE
 // Developer tracing (built only with -DMLA_TRACE): %globaltimer stamps per
 // tile and role for two pairs (the first and the middle one), read back
-// with mla_debug_read_trace.  Events: 0 producer issued the tile's loads,
-// 0 S: tile maximum agreed / V: producer issued the tile's loads, 1 MMA warp
+// with mla_debug_read_trace.  Events: 0 S: tile maximum agreed / V: producer issued the tile's loads, 1 MMA warp
 // saw the tile's data, 2 S: QK^T issued / V: first P half arrived, 3 S:
 // softmax exponentials done / V: PV issued, 4 S: softmax saw S / V: first
 // half's MMAs issued, 5 S: P buffer free, 6 S: P sent, 7 per segment: S query
-// loaded / V epilogue done.
-constexpr int kTraceTiles = 512, kTraceEvents = 8, kTracePairs = 2;
+// loaded / V epilogue done, 8 S producer issued the tile's load, 9 S issuer
+// passed its score-buffer wait.
+constexpr int kTraceTiles = 512, kTraceEvents = 10, kTracePairs = 2;
 __device__ unsigned long long g_trace[kTracePairs][2][kTraceEvents][kTraceTiles];
 // per CTA: kernel entry, range start (after setup), end of work
 __device__ unsigned long long g_trace_cta[2 * kMaxPairs][3];
@@ -360,9 +360,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     misc->bad_smem = (ptx::smem_u32(smem) & 1023u) != 0;
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(&bars->full[s], 1);
-      ptx::mbar_init(&bars->empty[s], isS ? 2 : 1);  // S: both QK^T issuers read a stage
+      ptx::mbar_init(&bars->empty[s], 1);
     }
-    for (int s = 0; s < 12; ++s) {
+    for (int s = 0; s < 6; ++s) {
       ptx::mbar_init(&bars->s_full[s], 1);
       ptx::mbar_init(&bars->s_free[s], 128);
     }
@@ -561,7 +561,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         int blk = cur.at(lt, lane);
         if (blk < 0 || blk >= a.num_blocks) blk = 0;  // reported by the softmax warps
         if (lane == 0) {
-          if (!isS) MLA_TRACE_EV(0, g);
+          if (!isS) MLA_TRACE_EV(0, g); else MLA_TRACE_EV(8, g);
           uint8_t *dst = smem + kOffRing + st * stage_bytes;
           uint64_t *fb = isS ? &bars->sfull[g % 6] : &bars->full[st];
           // the whole stage in one copy: nbox boxes of 64 rows x 128 B
@@ -577,10 +577,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         wait_bar_warp(&bars->empty[k % kStages], (k / kStages) & 1, abort);
   } else if (isS && (warp == 1 || warp == 6)) {
     // ========== S-CTA: QK^T issuers ==========
-    // Both issue every tile, each half of its 36 k-steps into its own partial
-    // score buffer (warp 1: latent boxes 0-3 and half of box 4, warp 6: the
-    // rest and the RoPE box); the softmax adds the two.  One thread alone
-    // cannot issue N=64 MMAs at the tensor pipe's rate, two can.
+    // The two issuers take alternate tiles (warp 1 even, warp 6 odd), each
+    // all 36 k-steps of its tile into score buffer g % 3.  One thread alone
+    // cannot issue N=64 MMAs at the tensor pipe's rate; two interleaved
+    // whole-tile chains come closer than two half-K chains into separate
+    // partial buffers, and the softmax reads one buffer per tile.
     if (lane == 0) {
       const int mine = warp == 1 ? 0 : 1;
       const uint32_t idesc = ptx::idesc_bf16(128, kTile, false, false);
@@ -594,30 +595,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         ptx::tc_fence_after();
         r += 2;  // the segment's query stages
         for (int lt = lt0; lt < lt1; ++lt, ++g, ++r) {
-          const int st = r % kStages, sb = (2 * g + mine) % 3;
+          if ((g & 1) != mine) continue;
+          const int st = r % kStages, sb = g % 3;
           if (!wait_bar(&bars->sfull[g % 6], (g / 6) & 1, abort)) { failed = true; break; }
-          if (mine == (g & 1)) MLA_TRACE_EV(1, g);
-          // partial buffer sb last held partial 2g+mine-3: tile g-2's second
-          // (for warp 1) or tile g-1's first (for warp 6), released as soon
-          // as the softmax has read that one partial
-          const int gp = g - 2 + mine;
-          if (gp >= 0 && !wait_bar(&bars->s_free[2 * (gp % 6) + (1 - mine)], (gp / 6) & 1, abort)) {
+          MLA_TRACE_EV(1, g);
+          // buffer sb last held tile g-3 (the other issuer's, read by the
+          // other softmax group)
+          const int gp = g - 3;
+          if (gp >= 0 && !wait_bar(&bars->s_free[gp % 6], (gp / 6) & 1, abort)) {
             failed = true;
             break;
           }
+          MLA_TRACE_EV(9, g);
           ptx::tc_fence_after();
           const uint32_t d = tmem + kTmemS + sb * kTile;
           const uint64_t bs = ring_desc + (uint64_t)((st * kSStage) >> 4);
 #pragma unroll
-          for (int j = 0; j < 18; ++j) {  // 9 boxes (8 latent + RoPE) x 4 k-steps of 16
-            const int kk = 18 * mine + j;
+          for (int kk = 0; kk < 36; ++kk)  // 9 boxes (8 latent + RoPE) x 4 k-steps of 16
             ptx::mma_bf16_ts(d, tmem + kTmemQ + kk * 8,
                              bs + (uint64_t)((((kk >> 2) * kBox) + (kk & 3) * 32) >> 4), idesc,
-                             j != 0);
-          }
-          ptx::mma_commit(&bars->s_full[2 * (g % 6) + mine]);
+                             kk != 0);
+          ptx::mma_commit(&bars->s_full[g % 6]);
           ptx::mma_commit(&bars->empty[st]);
-          if (mine == (g & 1)) MLA_TRACE_EV(2, g);
+          MLA_TRACE_EV(2, g);
         }
         if (failed) break;
         ptx::mma_commit(&bars->q_free);
@@ -798,95 +798,72 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // every row is copied once q_full completes: the stages go back
         if (threadIdx.x == (grp ? 224 : 64)) {
           if (wait_bar(&bars->q_full, seg & 1, abort)) {
-            for (int i = 0; i < 2; ++i) {  // stands for both issuers' releases
-              ptx::mbar_arrive(&bars->empty[rq % kStages]);
-              ptx::mbar_arrive(&bars->empty[(rq + 1) % kStages]);
-            }
+            ptx::mbar_arrive(&bars->empty[rq % kStages]);
+            ptx::mbar_arrive(&bars->empty[(rq + 1) % kStages]);
           }
         }
       }
 
       // this group's row sum over its tiles of the segment, relative to m_mine
       float m_mine = -INFINITY, l_mine = 0.f;
-      // Software pipeline: a tile's maximum is published as soon as its
-      // scores are read, before this group ships the P of its previous tile
-      // (held in registers), so the other group never waits on a transfer.
-      uint32_t pk_prev[32];
-      float alpha_prev = 1.f;
-      bool resc_prev = false;
-      int g_prev = -1;
-      // The previous tile's P leaves in two halves, each followed by half of
-      // this tile's exponentials, so the transfer overlaps the arithmetic.
+      // A tile's maximum is published as soon as its scores are read; its P
+      // leaves in two halves, each right after its 32 exponentials, so the
+      // first half is in flight while the second is computed.
+      uint32_t pk[32];
+      float alpha_tx = 1.f;  // the tile in flight: its rescale factor, flag and index
+      bool resc_tx = false;
+      int gt = -1;           // -1 once both halves have left
       auto send_half = [&](int half) -> bool {
-        if (g_prev < 0) return true;
+        if (gt < 0) return true;
         const uint32_t prow = rP + row * 128;
-        const int ph = ((g_prev >> 1) - 1) & 1;
-        // each half of buffer grp was last read by the V-CTA's PV of tile g_prev-2
-        if (g_prev >= 2 && !wait_bar_warp(&bars->p_free[2 * grp + half], ph, abort, true)) return false;
+        const int ph = ((gt >> 1) - 1) & 1;
+        // each half of buffer grp was last read by the V-CTA's PV of tile gt-2
+        if (gt >= 2 && !wait_bar_warp(&bars->p_free[2 * grp + half], ph, abort, true)) return false;
         if (half == 1) {  // tokens 32-63
 #pragma unroll
           for (int cc = 4; cc < 8; ++cc)
-            ptx::st_async_v4(prow + ((cc ^ (lane & 7)) << 4), pk_prev[4 * cc], pk_prev[4 * cc + 1],
-                             pk_prev[4 * cc + 2], pk_prev[4 * cc + 3], rPFullB);
-          if (lane == 0 && wq == 0) MLA_TRACE_EV(6, g_prev);
-          g_prev = -1;
+            ptx::st_async_v4(prow + ((cc ^ (lane & 7)) << 4), pk[4 * cc], pk[4 * cc + 1],
+                             pk[4 * cc + 2], pk[4 * cc + 3], rPFullB);
+          if (lane == 0 && wq == 0) MLA_TRACE_EV(6, gt);
+          gt = -1;
           return true;
         }
         // half 0 (tokens 0-31) with the rescale factors and flags
-        if (lane == 0 && wq == 0) MLA_TRACE_EV(5, g_prev);
+        if (lane == 0 && wq == 0) MLA_TRACE_EV(5, gt);
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc)
-          ptx::st_async_v4(prow + ((cc ^ (lane & 7)) << 4), pk_prev[4 * cc], pk_prev[4 * cc + 1],
-                           pk_prev[4 * cc + 2], pk_prev[4 * cc + 3], rPFullA);
+          ptx::st_async_v4(prow + ((cc ^ (lane & 7)) << 4), pk[4 * cc], pk[4 * cc + 1],
+                           pk[4 * cc + 2], pk[4 * cc + 3], rPFullA);
         {  // the warp's 32 factors as 8 vector stores (lanes 0-7)
           float a4[4];
 #pragma unroll
-          for (int j = 0; j < 4; ++j) a4[j] = __shfl_sync(0xffffffffu, alpha_prev, (4 * lane + j) & 31);
+          for (int j = 0; j < 4; ++j) a4[j] = __shfl_sync(0xffffffffu, alpha_tx, (4 * lane + j) & 31);
           if (lane < 8)
             ptx::st_async_v4(rAux + (32 * wq + 4 * lane) * 4, __float_as_uint(a4[0]),
                              __float_as_uint(a4[1]), __float_as_uint(a4[2]), __float_as_uint(a4[3]),
                              rPFullA);
         }
-        const uint32_t wflag = __ballot_sync(0xffffffffu, resc_prev);
+        const uint32_t wflag = __ballot_sync(0xffffffffu, resc_tx);
         if (lane == 0) ptx::st_async_b32(rAux + 512 + wq * 4, wflag, rPFullA);
         return true;
       };
-      auto send_prev = [&]() -> bool { return send_half(0) && send_half(1); };
       for (int lt = lt0; lt < lt1; ++lt, ++g) {
         if ((g & 1) != grp) continue;
-        const int sb0 = (2 * g) % 3, sb1 = (2 * g + 1) % 3;
-        // the first partial is read (and its buffer handed back to the
-        // second issuer's next tile) before the second is waited for
-        if (!wait_bar_warp(&bars->s_full[2 * (g % 6)], (g / 6) & 1, abort)) { failed = true; break; }
+        const int sb = g % 3;
+        if (!wait_bar_warp(&bars->s_full[g % 6], (g / 6) & 1, abort)) { failed = true; break; }
         if (lane == 0 && wq == 0) MLA_TRACE_EV(4, g);
         ptx::tc_fence_after();
         float s[64];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           float v[16];
-          ptx::tmem_ld16(tmem + lane_base + kTmemS + sb0 * kTile + q * 16, v);
+          ptx::tmem_ld16(tmem + lane_base + kTmemS + sb * kTile + q * 16, v);
 #pragma unroll
           for (int i = 0; i < 16; ++i) s[q * 16 + i] = v[i];
         }
         ptx::tmem_ld_wait();
         ptx::tc_fence_before();
-        ptx::mbar_arrive(&bars->s_free[2 * (g % 6)]);
-        if (!wait_bar_warp(&bars->s_full[2 * (g % 6) + 1], (g / 6) & 1, abort)) { failed = true; break; }
-        ptx::tc_fence_after();
-#pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {  // the second partial, 32 columns at a time
-          float v[2][16];
-#pragma unroll
-          for (int q = 0; q < 2; ++q)
-            ptx::tmem_ld16(tmem + lane_base + kTmemS + sb1 * kTile + (2 * h2 + q) * 16, v[q]);
-          ptx::tmem_ld_wait();
-#pragma unroll
-          for (int q = 0; q < 2; ++q)
-#pragma unroll
-            for (int i = 0; i < 16; ++i) s[(2 * h2 + q) * 16 + i] += v[q][i];
-        }
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(&bars->s_free[2 * (g % 6) + 1]);
+        ptx::mbar_arrive(&bars->s_free[g % 6]);  // the buffer goes back to tile g+3
         const int tok0 = lt * kTile;
         if (tok0 + kTile > n_vis) {
 #pragma unroll
@@ -915,22 +892,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (lane == 0 && wq == 0) MLA_TRACE_EV(0, g);
         float ls[2] = {0.f, 0.f};
         bool sent = true;
+        alpha_tx = alpha;
+        resc_tx = resc;
+        gt = g;
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
-          sent = sent && send_half(half);  // frees pk_prev[16*half ..]
 #pragma unroll
           for (int i = 16 * half; i < 16 * half + 16; ++i) {
             const float p0 = ptx::ex2(fmaf(s[2 * i], c, -m_use));
             const float p1 = ptx::ex2(fmaf(s[2 * i + 1], c, -m_use));
             ls[i & 1] += p0 + p1;
-            pk_prev[i] = ptx::pack_bf16x2(p0, p1);
+            pk[i] = ptx::pack_bf16x2(p0, p1);
           }
+          sent = sent && send_half(half);
         }
         if (!sent) { failed = true; break; }
         const float lsum = ls[0] + ls[1];
-        alpha_prev = alpha;
-        resc_prev = resc;
-        g_prev = g;
         if (m_use != m_mine) {  // the maximum moved since this group's last tile
           l_mine = (m_mine == -INFINITY) ? 0.f : l_mine * ptx::ex2(m_mine - m_use);
           m_mine = m_use;
@@ -938,7 +915,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         l_mine += lsum;
         if (lane == 0 && wq == 0) MLA_TRACE_EV(3, g);
       }
-      if (!failed && !send_prev()) failed = true;
+      // Nothing is pending here (both halves of every tile left inside the
+      // loop), so this returns at once; without the call the compiler's
+      // allocation spills registers in the loop above.
+      if (!failed && !(send_half(0) && send_half(1))) failed = true;
       if (failed) break;
       // -- segment end: merge the two groups' row sums, statistics -> V-CTA --
       if (seg > 0 && !wait_bar_warp(&bars->stats_free, (seg - 1) & 1, abort, true)) { failed = true; break; }
