@@ -281,9 +281,10 @@ int read_and_clear_gemm_error() {
 namespace {
 
 constexpr uint32_t kWholeA = 128 * 512 * 2;  // one head's weight, 128 KB
+constexpr int kWholeThreads = 256;
 
 template <bool kAbsorb>
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(kWholeThreads, 1)
     head_whole_kernel(const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmB, __nv_bfloat16 *out, int rows,
                       int Nt, int H) {
@@ -349,26 +350,48 @@ __global__ void __launch_bounds__(128, 1)
   }
   __syncwarp();
 
-  // ---- epilogue: TMEM -> bf16 global, thread = output column (c or a) ----
+  // ---- epilogue: TMEM -> bf16 global ----
+  // Lane = output column (c or a), TMEM column = query row.  Each M tile is
+  // transposed through the weight's (now idle) shared memory into [row][128]
+  // bf16, then every row leaves as 256 contiguous bytes (16-byte stores).
   const bool ok = ptx::mbar_wait(&done, 0);
   ptx::tc_fence_after();
   if (!ok || fail) atomicExch(&fail, 1);
-  if (ok && !fail) {
+  __syncthreads();  // every thread has seen `fail`; the MMAs are done with sA
+  if (!fail) {
     const int width = kAbsorb ? 512 : 128;
     const size_t row_stride = (size_t)H * width;
+    const int lane = threadIdx.x & 31, quad = warp & 3, half = warp >> 2;
+    const int nchunks = Nt / 16;  // 16 query rows per TMEM load
     for (int m = 0; m < kMTiles; ++m) {
-      __nv_bfloat16 *dst = out + (size_t)h * width + m * 128 + warp * 32 + (threadIdx.x & 31);
-      for (int c0 = 0; c0 < Nt; c0 += 16) {
-        float v[16];
-        ptx::tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + m * Nt + c0, v);
+      __nv_bfloat16 *stage = reinterpret_cast<__nv_bfloat16 *>(sA) + (size_t)m * Nt * 128;
+      // warps q and q + 4 share TMEM lanes 32q..32q+31 and take alternate
+      // 16-row chunks, four loads in flight per wait
+      for (int j0 = half; j0 < nchunks; j0 += 8) {
+        float v[4][16];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (j0 + 2 * u < nchunks)
+            ptx::tmem_ld16(tmem + ((uint32_t)(quad * 32) << 16) + m * Nt + (j0 + 2 * u) * 16, v[u]);
         ptx::tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int n = n0 + c0 + i;
-          if (n < rows) dst[(size_t)n * row_stride] = __float2bfloat16_rn(v[i]);
-        }
+        for (int u = 0; u < 4; ++u)
+          if (j0 + 2 * u < nchunks)
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              stage[(size_t)((j0 + 2 * u) * 16 + i) * 128 + quad * 32 + lane] =
+                  __float2bfloat16_rn(v[u][i]);
       }
     }
+    __syncthreads();
+    // thread t stores 16-byte piece t % 16 of rows t / 16, t / 16 + 16, ...
+    const int nrows = min(Nt, rows - n0), k = threadIdx.x & 15;
+    for (int m = 0; m < kMTiles; ++m)
+      for (int r = threadIdx.x >> 4; r < nrows; r += kWholeThreads / 16) {
+        const uint4 x = reinterpret_cast<const uint4 *>(sA)[((size_t)m * Nt + r) * 16 + k];
+        __nv_bfloat16 *dst = out + (size_t)(n0 + r) * row_stride + (size_t)h * width + m * 128;
+        reinterpret_cast<uint4 *>(dst)[k] = x;
+      }
   }
   ptx::tc_fence_before();
   __syncthreads();
@@ -390,7 +413,7 @@ cudaError_t launch_head_whole(const CUtensorMap &tmA, const CUtensorMap &tmB, vo
   pdl[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(H, (rows + Nt - 1) / Nt, 1);
-  cfg.blockDim = dim3(128, 1, 1);
+  cfg.blockDim = dim3(kWholeThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cfg.attrs = pdl;
