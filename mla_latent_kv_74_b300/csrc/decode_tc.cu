@@ -529,6 +529,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     int item, lt0, lt1, n_vis, g = 0;
     bool whole, failed = false;
     TableWindow cur;
+    const uint64_t evict_first = ptx::l2_policy_evict_first();
     const uint32_t stage_bytes = isS ? kSStage : kVStage;
     const int nbox = isS ? 9 : 8;
     int r = 0;  // ring position (tiles, plus two query stages per S segment)
@@ -564,9 +565,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (!isS) MLA_TRACE_EV(0, g); else MLA_TRACE_EV(8, g);
           uint8_t *dst = smem + kOffRing + st * stage_bytes;
           uint64_t *fb = isS ? &bars->sfull[g % 6] : &bars->full[st];
-          // the whole stage in one copy: nbox boxes of 64 rows x 128 B
+          // the whole stage in one copy: nbox boxes of 64 rows x 128 B; the
+          // V-CTA's copy is the last read of these lines, so it marks them
+          // first to be evicted from L2
           ptx::mbar_arrive_expect_tx(fb, nbox * kBox);
-          ptx::tma_load_3d(dst, isS ? &tm_cache : &tm_cache_v, fb, 0, blk * kTile, 0);
+          if (isS)
+            ptx::tma_load_3d(dst, &tm_cache, fb, 0, blk * kTile, 0);
+          else
+            ptx::tma_load_3d_hint(dst, &tm_cache_v, fb, 0, blk * kTile, 0, evict_first);
         }
       }
     }
@@ -1047,9 +1053,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
         }
       };
+      // the same for a split piece, stored with an evict-last L2 hint so the
+      // combine kernel finds it in L2 after the rest of the cache stream
+      auto flush_piece_keep = [&](const uint32_t (&pk)[32], size_t byte_off) {
+        __syncwarp();
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc)
+          *reinterpret_cast<uint4 *>(stg + lane * 128 + ((cc ^ (lane & 7)) << 4)) =
+              make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+        __syncwarp();
+        const uint64_t keep = ptx::l2_policy_evict_last();
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int r = 4 * i + (lane >> 3), k = lane & 7;
+          if (r < rows_here) {
+            const uint4 x = *reinterpret_cast<const uint4 *>(stg + r * 128 + ((k ^ (r & 7)) << 4));
+            ptx::st_global_v4_hint(dst_base + r * dst_row_bytes + byte_off + k * 16, x, keep);
+          }
+        }
+      };
 #pragma unroll 1
-      for (int q = 0; q < kDc / 64; ++q) {  // 64 TMEM columns per wait
-        float v[64];
+      // the next 64 columns load from TMEM while this piece is stored
+      float v[64];
+      auto load64 = [&](int q) {
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           float t16[16];
@@ -1057,18 +1083,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 16; ++i) v[u * 16 + i] = t16[i];
         }
-        ptx::tmem_ld_wait();
+      };
+      load64(0);
+      ptx::tmem_ld_wait();
+#pragma unroll 1
+      for (int q = 0; q < kDc / 64; ++q) {
         uint32_t pk[32];
-        if (whole) {  // 64 bf16 = one 128-byte piece
 #pragma unroll
-          for (int i = 0; i < 32; ++i) pk[i] = ptx::pack_bf16x2(v[2 * i] * inv_l, v[2 * i + 1] * inv_l);
+        for (int i = 0; i < 32; ++i) pk[i] = ptx::pack_bf16x2(v[2 * i] * inv_l, v[2 * i + 1] * inv_l);
+        if (q + 1 < kDc / 64) load64(q + 1);
+        if (whole)
           flush_piece(pk, (size_t)q * 128);
-        } else {  // a split piece: the same bf16 piece into o_part (two branches
-                  // on purpose: one branch costs the main loops registers)
-#pragma unroll
-          for (int i = 0; i < 32; ++i) pk[i] = ptx::pack_bf16x2(v[2 * i] * inv_l, v[2 * i + 1] * inv_l);
-          flush_piece(pk, (size_t)q * 128);
-        }
+        else
+          flush_piece_keep(pk, (size_t)q * 128);
+        ptx::tmem_ld_wait();
       }
       if (whole) {
         if (row < a.H) a.lse[grow] = seg_bad ? -INFINITY : lse_val;
