@@ -1072,7 +1072,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
         }
       };
-#pragma unroll 1
       // the next 64 columns load from TMEM while this piece is stored
       float v[64];
       auto load64 = [&](int q) {
