@@ -12,27 +12,28 @@
 // latent accumulator O (128 heads x 512) or the full query, not both:
 //   * the S-CTA (cluster rank 1) keeps the item's query [q_lat ; q_rope]
 //     (128 x 576 bf16 = 288 columns) in TMEM as the A operand of
-//     S = Q C^T (M=128, N=64, K=576; three 64-column partial-score buffers
-//     in the other columns), runs the online softmax and ships P (bf16) to
-//     its peer;
+//     S = Q C^T (M=128, N=64, K=576; three 64-column score buffers, one
+//     per tile in flight, in the other columns), runs the online softmax and
+//     ships P (bf16) to its peer;
 //   * the V-CTA (rank 0) keeps O (512 columns) in TMEM and accumulates
 //     O += P C (M=128, N=2x256, K=64) with P in its shared memory.
 // Each CTA streams the cache through its own ring of shared-memory stages,
 // one 3-D TMA copy per stage: the S-CTA loads [c_KV ; k_R] tiles (HBM) and
 // frees a stage as soon as its QK^T is done; the V-CTA loads the latent part
-// of the same tiles a little later (L2 hits) and frees a stage after its PV.
-// Decoupling the rings keeps the long HBM latency off the softmax -> PV
-// chain.  Each segment's query reaches the S-CTA through its ring too (two
+// of the same tiles a little later (L2 hits, issued evict-first: it is the
+// lines' last read) and frees a stage after its PV.  Decoupling the rings
+// keeps the long HBM latency off the softmax -> PV chain.  Each segment's query reaches the S-CTA through its ring too (two
 // stages ahead of the segment's tiles), copied into TMEM by a softmax group.
-// Two warps of the S-CTA each issue half of every tile's k-steps into their
-// own partial-score buffer (one thread cannot issue N = 64 MMAs at the
-// tensor pipe's rate, two can); the softmax adds the two partials.
+// Two warps of the S-CTA issue QK^T on alternate tiles, all 36 k-steps of a
+// tile into its score buffer (one thread issues an N = 64 MMA only every
+// ~80 cycles; two interleaved chains reach ~45).
 //
 // P goes straight into the V-CTA's shared memory by st.async (distributed
 // shared memory, counted on the destination mbarrier), already in the
 // 128B-swizzled K-major layout of the MMA operand, with the rows' rescale
 // factors and four per-warp rescale flags; one P buffer per tile parity.
-// Two groups of four softmax warps take alternate tiles, so one group's
+// Each half (32 tokens) leaves as soon as its exponentials are done.  Two
+// groups of four softmax warps take alternate tiles, so one group's
 // transfer overlaps the other's exponentials.  The groups agree on the
 // running maximum through shared memory (a tile's maximum is published
 // before its exponentials, so the next tile waits only for that), keep
@@ -48,9 +49,9 @@
 //
 // Split-KV: the visible tiles of all (sequence, slot) items are laid end to
 // end and cut into equal ranges, one per co-resident pair.  Pieces of items
-// cut by a range boundary write fp32 partials (O/l and lse) that
-// combine_tc_kernel merges with log-sum-exp weights; whole items are written
-// directly.  The plan is computed on the device from seqlens (no host sync).
+// cut by a range boundary write partials (bf16 O/l, stored evict-last so
+// they stay in L2, and fp32 lse) that combine_tc_kernel merges with
+// log-sum-exp weights; whole items are written directly.  The plan is computed on the device from seqlens (no host sync).
 // With several query slots per sequence the items are laid out slot by slot
 // and each slot gets its own equal share of the pairs, so pair j of every
 // slot walks the same sequences' pages at the same time: the slots after the
@@ -58,9 +59,9 @@
 // reading the cache from HBM again.
 //
 // Warp roles (352 threads per CTA): warp 0 TMA producer, warp 1 TMEM owner
-// and MMA issuer; S-CTA: warp 6 second QK^T issuer, warps 2-5 and 7-10 the
-// two softmax groups (even / odd tiles); V-CTA: warps 2-5 rescale and
-// epilogue.  A warp w that touches TMEM owns lanes 32*(w%4) .. 32*(w%4)+31.
+// and MMA issuer; S-CTA: warp 6 the second QK^T issuer (warp 1 takes the
+// even tiles, warp 6 the odd ones), warps 2-5 and 7-10 the two softmax
+// groups (even / odd tiles); V-CTA: warps 2-5 rescale and epilogue.  A warp w that touches TMEM owns lanes 32*(w%4) .. 32*(w%4)+31.
 // The kernel is launched as a programmatic dependent of the previous kernel
 // in the stream and waits for it only after its barrier and TMEM setup.
 //
