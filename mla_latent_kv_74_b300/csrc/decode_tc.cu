@@ -1252,7 +1252,30 @@ __global__ void __launch_bounds__(32 * kCombineRows) combine_tc_kernel(DecodeArg
     const int p_l = base + lane;
     const float wl = p_l <= p1 ? expf(a.lse_part[(size_t)slot_of(p_l) * 128 + h] - mx) * inv : 0.f;
     const int n = min(32, p1 - base + 1);
-    for (int j = 0; j < n; ++j) {
+    int j = 0;
+    for (; j + 4 <= n; j += 4) {  // four pieces' loads in flight at once
+      uint4 x[4][2];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(
+                               a.o_part + ((size_t)slot_of(base + j + u) * 128 + h) * kDc) +
+                           lane * 2;
+        x[u][0] = src[0];
+        x[u][1] = src[1];
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float wgt = __shfl_sync(0xffffffffu, wl, j + u);
+        const uint32_t wd[8] = {x[u][0].x, x[u][0].y, x[u][0].z, x[u][0].w,
+                                x[u][1].x, x[u][1].y, x[u][1].z, x[u][1].w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          acc[2 * i] = fmaf(wgt, __uint_as_float(wd[i] << 16), acc[2 * i]);
+          acc[2 * i + 1] = fmaf(wgt, __uint_as_float(wd[i] & 0xffff0000u), acc[2 * i + 1]);
+        }
+      }
+    }
+    for (; j < n; ++j) {
       const float wgt = __shfl_sync(0xffffffffu, wl, j);
       float v[16];
       load_piece16(a.o_part + ((size_t)slot_of(base + j) * 128 + h) * kDc, lane, v);
