@@ -252,6 +252,43 @@ mla_status mla_decode(const void *q_lat, const void *q_rope, const void *cache,
                       float *lse, void *workspace, size_t workspace_bytes,
                       mla_stream_t stream);
 
+/* mla_decode restricted to the logical cache blocks [first_block, end_block)
+ * of every sequence: the keys j with first_block*block_size <= j <
+ * end_block*block_size (and j < n as above).  o_lat and lse are then the
+ * softmax-weighted latent and the log-sum-exp over those keys alone (o_lat
+ * = 0, lse = -inf where none is visible), i.e. one piece of a split-KV
+ * computation; pieces over disjoint ranges that cover [0, n) merge into
+ * mla_decode's result with mla_combine_pieces.  This is how one very long
+ * sequence is split across GPUs: each GPU decodes the blocks it holds and
+ * the pieces are gathered to one of them.  block_table rows keep their
+ * full width (entries before first_block are not read).  Arguments, layouts
+ * and workspace as for mla_decode; first_block < 0 or end_block <
+ * first_block returns MLA_ERR_INVALID_ARG.  Only the tensor-core path
+ * takes block ranges (other problems return MLA_ERR_UNSUPPORTED). */
+mla_status mla_decode_blocks(const void *q_lat, const void *q_rope, const void *cache,
+                             int num_blocks, const int32_t *block_table, int max_blocks,
+                             const int32_t *seqlens, int max_seqlen, int B, int Hq,
+                             int first_block, int end_block, const mla_dims *dims,
+                             void *o_lat, float *lse, void *workspace, size_t workspace_bytes,
+                             mla_stream_t stream);
+
+/* Log-sum-exp merge of P pieces of the same rows, each the output of
+ * mla_decode_blocks over one range of a partition of the keys:
+ *   lse = ln sum_p exp(lse_p),   o_lat = sum_p exp(lse_p - lse) o_p
+ * (the softmax over the union of the ranges, "Part 3" 2.a and 3.f, written
+ * as a weighted mean of the per-range means).  Pieces with lse_p = -inf
+ * weigh nothing; rows with every lse_p = -inf (or a NaN) get o_lat = 0,
+ * lse = -inf.
+ *   o_pieces   [P, B, Hq, H, d_c] bf16   input (pieces stacked, 16-byte aligned)
+ *   lse_pieces [P, B, Hq, H] float32     input
+ *   o_lat      [B, Hq, H, d_c] bf16      output
+ *   lse        [B, Hq, H] float32        output
+ * Supported: the tensor-core decode shapes (bf16, d_c = 512); others return
+ * MLA_ERR_UNSUPPORTED.  Asynchronous on `stream`; needs no workspace. */
+mla_status mla_combine_pieces(const void *o_pieces, const float *lse_pieces, int P, int B,
+                              int Hq, const mla_dims *dims, void *o_lat, float *lse,
+                              mla_stream_t stream);
+
 /* Expand the latent output through W_UV: out[b,i,h,:] = W_UV[h] o_lat[b,i,h,:].
  * ("From Vanilla Transformers to Modern LLMs -- Part 3" 3.g; "MLA, dim by
  *  dim" 4.2, the value chain contracted left to right.)

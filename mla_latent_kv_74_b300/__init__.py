@@ -45,6 +45,8 @@ EXPORTED = (
     "mla_append_cache",
     "mla_decode_workspace_size",
     "mla_decode",
+    "mla_decode_blocks",
+    "mla_combine_pieces",
     "mla_out_proj",
     "mla_get_error",
     "mla_status_string",
@@ -101,6 +103,8 @@ def _load():
         "mla_append_cache": [P, I, P, I, P, P, P, I, I, D, P],
         "mla_decode_workspace_size": [I, I, I, D, ctypes.POINTER(Z)],
         "mla_decode": [P, P, P, I, P, I, P, I, I, I, D, P, P, P, Z, P],
+        "mla_decode_blocks": [P, P, P, I, P, I, P, I, I, I, I, I, D, P, P, P, Z, P],
+        "mla_combine_pieces": [P, P, I, I, I, D, P, P, P],
         "mla_out_proj": [P, P, P, I, I, D, P],
         "mla_get_error": [P, P],
         "mla_status_string": [I],
@@ -254,6 +258,28 @@ def mla_decode(q_lat, q_rope, cache, num_blocks, block_table, seqlens, max_seqle
                            int(max_seqlen), B, Hq, ctypes.byref(dims), _ptr(o_lat), _ptr(lse),
                            _ptr(workspace), workspace.numel() * workspace.element_size(),
                            _stream(stream)), "mla_decode")
+
+
+def mla_decode_blocks(q_lat, q_rope, cache, num_blocks, block_table, seqlens, max_seqlen,
+                      first_block, end_block, dims: Dims, o_lat, lse, workspace, stream=None):
+    """``mla_decode`` over the cache blocks ``[first_block, end_block)`` of every
+    sequence: one split-KV piece (``o_lat``, ``lse`` over those keys alone)."""
+    B, Hq = q_lat.shape[0], q_lat.shape[1]
+    _check(_lib.mla_decode_blocks(_ptr(q_lat), _ptr(q_rope), _ptr(cache), int(num_blocks),
+                                  _ptr(block_table), block_table.shape[1], _ptr(seqlens),
+                                  int(max_seqlen), B, Hq, int(first_block), int(end_block),
+                                  ctypes.byref(dims), _ptr(o_lat), _ptr(lse), _ptr(workspace),
+                                  workspace.numel() * workspace.element_size(),
+                                  _stream(stream)), "mla_decode_blocks")
+
+
+def mla_combine_pieces(o_pieces, lse_pieces, dims: Dims, o_lat, lse, stream=None):
+    """Merge ``P`` stacked pieces ``[P,B,Hq,H,d_c]`` / ``[P,B,Hq,H]`` (outputs of
+    ``mla_decode_blocks`` over disjoint ranges) into ``o_lat`` and ``lse``."""
+    P, B, Hq = o_pieces.shape[0], o_pieces.shape[1], o_pieces.shape[2]
+    _check(_lib.mla_combine_pieces(_ptr(o_pieces), _ptr(lse_pieces), P, B, Hq,
+                                   ctypes.byref(dims), _ptr(o_lat), _ptr(lse), _stream(stream)),
+           "mla_combine_pieces")
 
 
 def mla_out_proj(o_lat, W_UV, out, dims: Dims, stream=None):

@@ -3,6 +3,8 @@
 // device kernels never allocate and never synchronise.
 #include <math.h>
 
+#include <climits>
+
 #include "internal.cuh"
 #include "tc.cuh"
 
@@ -193,15 +195,20 @@ MLA_API mla_status mla_decode_workspace_size(int B, int Hq, int max_seqlen, cons
   return MLA_OK;
 }
 
-MLA_API mla_status mla_decode(const void *q_lat, const void *q_rope, const void *cache,
-                              int num_blocks, const int32_t *block_table, int max_blocks,
-                              const int32_t *seqlens, int max_seqlen, int B, int Hq,
-                              const mla_dims *dims, void *o_lat, float *lse, void *workspace,
-                              size_t workspace_bytes, mla_stream_t stream) {
+namespace {
+
+// mla_decode and mla_decode_blocks: the same checks, then one launch.
+mla_status decode_call(const void *q_lat, const void *q_rope, const void *cache, int num_blocks,
+                       const int32_t *block_table, int max_blocks, const int32_t *seqlens,
+                       int max_seqlen, int B, int Hq, int first_block, int end_block,
+                       bool ranged, const mla_dims *dims, void *o_lat, float *lse,
+                       void *workspace, size_t workspace_bytes, mla_stream_t stream) {
   if (!dims_ok(dims)) return dims ? MLA_ERR_UNSUPPORTED : MLA_ERR_INVALID_ARG;
-  if (B < 0 || Hq < 1 || max_seqlen < 0 || num_blocks < 1 || max_blocks < 1)
+  if (B < 0 || Hq < 1 || max_seqlen < 0 || num_blocks < 1 || max_blocks < 1 ||
+      first_block < 0 || end_block < first_block)
     return MLA_ERR_INVALID_ARG;
   if ((long)B * Hq > kMaxDecodeItems) return MLA_ERR_UNSUPPORTED;
+  if (ranged && !tc_decode_supported(*dims, B, Hq)) return MLA_ERR_UNSUPPORTED;
   if (B == 0) return MLA_OK;
   if (!q_lat || !cache || !block_table || !seqlens || !o_lat || !lse ||
       (dims->d_r > 0 && !q_rope))
@@ -217,11 +224,50 @@ MLA_API mla_status mla_decode(const void *q_lat, const void *q_rope, const void 
   const float scale = eff_scale(dims);
   if (tc_decode_supported(*dims, B, Hq))
     return cuda_status(launch_decode_tc(q_lat, q_rope, cache, num_blocks, block_table,
-                                        max_blocks, seqlens, max_seqlen, B, Hq, *dims, scale,
-                                        o_lat, lse, workspace, st));
+                                        max_blocks, seqlens, max_seqlen, B, Hq, first_block,
+                                        end_block, *dims, scale, o_lat, lse, workspace, st));
   return cuda_status(launch_decode_simt(q_lat, q_rope, cache, num_blocks, block_table,
                                         max_blocks, seqlens, max_seqlen, B, Hq, *dims, scale,
                                         o_lat, lse, workspace, st));
+}
+
+}  // namespace
+
+MLA_API mla_status mla_decode(const void *q_lat, const void *q_rope, const void *cache,
+                              int num_blocks, const int32_t *block_table, int max_blocks,
+                              const int32_t *seqlens, int max_seqlen, int B, int Hq,
+                              const mla_dims *dims, void *o_lat, float *lse, void *workspace,
+                              size_t workspace_bytes, mla_stream_t stream) {
+  return decode_call(q_lat, q_rope, cache, num_blocks, block_table, max_blocks, seqlens,
+                     max_seqlen, B, Hq, 0, INT_MAX, false, dims, o_lat, lse, workspace,
+                     workspace_bytes, stream);
+}
+
+MLA_API mla_status mla_decode_blocks(const void *q_lat, const void *q_rope, const void *cache,
+                                     int num_blocks, const int32_t *block_table, int max_blocks,
+                                     const int32_t *seqlens, int max_seqlen, int B, int Hq,
+                                     int first_block, int end_block, const mla_dims *dims,
+                                     void *o_lat, float *lse, void *workspace,
+                                     size_t workspace_bytes, mla_stream_t stream) {
+  return decode_call(q_lat, q_rope, cache, num_blocks, block_table, max_blocks, seqlens,
+                     max_seqlen, B, Hq, first_block, end_block, true, dims, o_lat, lse,
+                     workspace, workspace_bytes, stream);
+}
+
+MLA_API mla_status mla_combine_pieces(const void *o_pieces, const float *lse_pieces, int P,
+                                      int B, int Hq, const mla_dims *dims, void *o_lat,
+                                      float *lse, mla_stream_t stream) {
+  if (!dims_ok(dims)) return dims ? MLA_ERR_UNSUPPORTED : MLA_ERR_INVALID_ARG;
+  if (P < 1 || B < 0 || Hq < 1) return MLA_ERR_INVALID_ARG;
+  if ((long)B * Hq > kMaxDecodeItems || !tc_decode_supported(*dims, B, Hq))
+    return MLA_ERR_UNSUPPORTED;
+  if (B == 0) return MLA_OK;
+  if (!o_pieces || !lse_pieces || !o_lat || !lse || !al(o_pieces, 16) || !al(lse_pieces, 4) ||
+      !al(o_lat, 16) || !al(lse, 4))
+    return MLA_ERR_INVALID_ARG;
+  const long rows = (long)B * Hq * dims->H;
+  return cuda_status(launch_combine_pieces_tc(o_pieces, lse_pieces, P, rows, o_lat, lse,
+                                              reinterpret_cast<cudaStream_t>(stream)));
 }
 
 MLA_API mla_status mla_prefill_workspace_size(int total_tokens, const mla_dims *dims,

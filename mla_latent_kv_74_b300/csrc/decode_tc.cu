@@ -175,6 +175,10 @@ struct DecodeArgs {
   const int32_t *block_table;
   const int32_t *seqlens;
   int B, Hq, H, max_blocks, max_seqlen, num_blocks, npairs;
+  // the call covers the tokens [tok0, tok0 + tok_len) of every sequence
+  // (0 and INT_MAX: all of them); block_table then starts at the range's
+  // first block, so tile i of an item is the range's i-th block
+  int tok0, tok_len;
   float scale_log2;
   __nv_bfloat16 *o_lat;
   float *lse;
@@ -221,7 +225,8 @@ __device__ __forceinline__ int visible_len(const DecodeArgs &a, int w, bool *bad
     *bad = true;
     return 0;
   }
-  const int n = sl - a.Hq + slot + 1;
+  int n = sl - a.Hq + slot + 1 - a.tok0;  // visible tokens from the range start
+  if (n > a.tok_len) n = a.tok_len;
   return n > 0 ? n : 0;
 }
 
@@ -1339,6 +1344,50 @@ int pairs_for_device() {
   return (limit > 0 && limit < n) ? limit : n;
 }
 
+// Log-sum-exp merge of P pieces of the same rows (the outputs of calls over
+// disjoint block ranges): one thread per 8 columns of an output row, four
+// pieces' loads in flight at a time.  A piece with lse = -inf (nothing
+// visible in its range) weighs nothing; rows with nothing visible in any
+// piece get o = 0, lse = -inf.
+__global__ void __launch_bounds__(256) combine_pieces_kernel(const __nv_bfloat16 *o_pieces,
+                                                             const float *lse_pieces, int P,
+                                                             long rows, __nv_bfloat16 *o_lat,
+                                                             float *lse) {
+  const long t = (long)blockIdx.x * 256 + threadIdx.x;
+  const long row = t / (kDc / 8);
+  const int c8 = (int)(t % (kDc / 8));
+  if (row >= rows) return;
+  uint4 *dst = reinterpret_cast<uint4 *>(o_lat + (size_t)row * kDc) + c8;
+  float mx = -INFINITY;
+  for (int p = 0; p < P; ++p) mx = fmaxf(mx, lse_pieces[(size_t)p * rows + row]);
+  if (!(mx > -INFINITY)) {  // nothing visible (or a NaN)
+    *dst = make_uint4(0, 0, 0, 0);
+    if (c8 == 0) lse[row] = -INFINITY;
+    return;
+  }
+  float sum = 0.f, acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+#pragma unroll 4
+  for (int p = 0; p < P; ++p) {
+    const float wgt = expf(lse_pieces[(size_t)p * rows + row] - mx);
+    const uint4 x = reinterpret_cast<const uint4 *>(o_pieces + ((size_t)p * rows + row) * kDc)[c8];
+    const uint32_t wd[4] = {x.x, x.y, x.z, x.w};
+    sum += wgt;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      acc[2 * i] = fmaf(wgt, __uint_as_float(wd[i] << 16), acc[2 * i]);
+      acc[2 * i + 1] = fmaf(wgt, __uint_as_float(wd[i] & 0xffff0000u), acc[2 * i + 1]);
+    }
+  }
+  const float inv = 1.f / sum;
+  *dst = make_uint4(ptx::pack_bf16x2(acc[0] * inv, acc[1] * inv),
+                    ptx::pack_bf16x2(acc[2] * inv, acc[3] * inv),
+                    ptx::pack_bf16x2(acc[4] * inv, acc[5] * inv),
+                    ptx::pack_bf16x2(acc[6] * inv, acc[7] * inv));
+  if (c8 == 0) lse[row] = mx + logf(sum);
+}
+
 }  // namespace
 
 #ifdef MLA_TRACE
@@ -1370,8 +1419,8 @@ size_t tc_decode_workspace_bytes(int B, int Hq, const mla_dims &) {
 cudaError_t launch_decode_tc(const void *q_lat, const void *q_rope, const void *cache,
                              int num_blocks, const int32_t *block_table, int max_blocks,
                              const int32_t *seqlens, int max_seqlen, int B, int Hq,
-                             const mla_dims &d, float scale, void *o_lat, float *lse,
-                             void *workspace, cudaStream_t st) {
+                             int first_block, int end_block, const mla_dims &d, float scale,
+                             void *o_lat, float *lse, void *workspace, cudaStream_t st) {
   char *ws = static_cast<char *>(workspace);
   __nv_bfloat16 *o_part = reinterpret_cast<__nv_bfloat16 *>(ws + kWsHeader);
   const uint64_t rows = (uint64_t)B * Hq * d.H;
@@ -1402,7 +1451,9 @@ cudaError_t launch_decode_tc(const void *q_lat, const void *q_rope, const void *
   DecodeArgs a;
   a.q_lat = static_cast<const __nv_bfloat16 *>(q_lat);
   a.q_rope = static_cast<const __nv_bfloat16 *>(q_rope);
-  a.block_table = block_table;
+  // a block range starts the table at its first block (no item has a tile
+  // when that is past the table's end, so the pointer is then never read)
+  a.block_table = block_table + (first_block < max_blocks ? first_block : max_blocks);
   a.seqlens = seqlens;
   a.B = B;
   a.Hq = Hq;
@@ -1411,6 +1462,13 @@ cudaError_t launch_decode_tc(const void *q_lat, const void *q_rope, const void *
   a.max_seqlen = max_seqlen;
   a.num_blocks = num_blocks;
   a.npairs = npairs;
+  {  // the range in tokens, clamped to the table (no sequence reaches past it)
+    const long b0 = first_block < max_blocks ? first_block : max_blocks;
+    const long b1 = end_block < max_blocks ? end_block : max_blocks;
+    const long t0 = b0 * kTile, tl = (b1 - b0) * kTile;
+    a.tok0 = t0 > INT_MAX ? INT_MAX : (int)t0;
+    a.tok_len = tl > INT_MAX ? INT_MAX : (int)tl;
+  }
   a.scale_log2 = scale * kLog2e;
   a.o_lat = static_cast<__nv_bfloat16 *>(o_lat);
   a.lse = lse;
@@ -1443,6 +1501,16 @@ cudaError_t launch_decode_tc(const void *q_lat, const void *q_rope, const void *
   cfg.blockDim = dim3(32 * kCombineRows, 1, 1);
   cfg.dynamicSmemBytes = 0;
   return cudaLaunchKernelEx(&cfg, combine_kernel, a);
+}
+
+cudaError_t launch_combine_pieces_tc(const void *o_pieces, const float *lse_pieces, int P,
+                                     long rows, void *o_lat, float *lse, cudaStream_t st) {
+  if (rows <= 0) return cudaSuccess;
+  const long threads = rows * (kDc / 8);
+  combine_pieces_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(
+      static_cast<const __nv_bfloat16 *>(o_pieces), lse_pieces, P, rows,
+      static_cast<__nv_bfloat16 *>(o_lat), lse);
+  return cudaGetLastError();
 }
 
 }  // namespace mla

@@ -16,11 +16,16 @@ cudaError_t launch_absorb_tc(const void *q_nope, const void *W_UK, void *q_lat, 
                              const mla_dims &d, cudaStream_t st);
 cudaError_t launch_out_proj_tc(const void *o_lat, const void *W_UV, void *out, int rows,
                                const mla_dims &d, cudaStream_t st);
+// Attention over the logical cache blocks [first_block, end_block) of every
+// sequence (0 and INT_MAX: the whole visible length).
 cudaError_t launch_decode_tc(const void *q_lat, const void *q_rope, const void *cache,
                              int num_blocks, const int32_t *block_table, int max_blocks,
                              const int32_t *seqlens, int max_seqlen, int B, int Hq,
-                             const mla_dims &d, float scale, void *o_lat, float *lse,
-                             void *workspace, cudaStream_t st);
+                             int first_block, int end_block, const mla_dims &d, float scale,
+                             void *o_lat, float *lse, void *workspace, cudaStream_t st);
+// Log-sum-exp merge of P pieces [P][rows][512] bf16 + [P][rows] fp32.
+cudaError_t launch_combine_pieces_tc(const void *o_pieces, const float *lse_pieces, int P,
+                                     long rows, void *o_lat, float *lse, cudaStream_t st);
 
 // bf16, d_c = 512, d_r = 64, d_model a multiple of 64 (fused latent / RoPE-key
 // projection into the paged cache on tcgen05).

@@ -249,6 +249,72 @@ def mla_decode(q_nope, q_rope, cache, block_table, seqlens, W_UK, W_UV, Hq,
     return out, o_lat, lse
 
 
+def mla_decode_blocks(q_nope, q_rope, cache, block_table, seqlens, W_UK, W_UV, Hq,
+                      first_block, end_block, scale=None, batch_indices=None,
+                      head_indices=None):
+    """The decode step over the keys of logical blocks ``[first_block,
+    end_block)`` only: position ``j`` takes part when ``first_block * bs <= j
+    < end_block * bs`` and ``j`` is visible to the query slot.  The softmax
+    is the same definition taken over that subset of the keys, so ``o_lat``
+    and ``lse`` are one split-KV piece; a row with no key in the range has
+    ``o = 0`` and ``lse = -inf``.  Shapes and returns as ``mla_decode``.
+    (Not on the pages: it splits the key set the softmax of "From Vanilla
+    Transformers to Modern LLMs -- Part 3" 2.a / 3.f runs over.)
+    """
+    q_nope = np.asarray(q_nope, np.float64)
+    q_rope = np.asarray(q_rope, np.float64)
+    W_UK = np.asarray(W_UK, np.float64)
+    W_UV = np.asarray(W_UV, np.float64)
+    B, _, H, d_h = q_nope.shape
+    d_c = W_UK.shape[2]
+    bs = cache.shape[1]
+    if scale is None:
+        scale = default_scale(d_h, q_rope.shape[3])
+    batch_indices = list(range(B) if batch_indices is None else batch_indices)
+    head_indices = list(range(H) if head_indices is None else head_indices)
+    lo = max(0, int(first_block)) * bs
+    hi = max(0, int(end_block)) * bs
+    out = np.zeros((len(batch_indices), Hq, len(head_indices), d_h))
+    o_lat = np.zeros((len(batch_indices), Hq, len(head_indices), d_c))
+    lse = np.full((len(batch_indices), Hq, len(head_indices)), -math.inf)
+    for ob, b in enumerate(batch_indices):
+        n_max = visible_length(seqlens[b], Hq, Hq - 1)
+        all_rows = gather_sequence(cache, block_table[b], n_max)
+        for oh, h in enumerate(head_indices):
+            for i in range(Hq):
+                n = visible_length(seqlens[b], Hq, i)
+                rows = all_rows[lo:min(n, hi)]
+                r = attention_row(q_nope[b, i, h], q_rope[b, i, h], rows, W_UK[h], W_UV[h],
+                                  scale, d_c)
+                out[ob, i, oh] = r["out"]
+                o_lat[ob, i, oh] = r["o_lat"]
+                lse[ob, i, oh] = r["lse"]
+    return out, o_lat, lse
+
+
+def combine_pieces(o_pieces, lse_pieces):
+    """Merge pieces computed over disjoint key sets: ``lse = ln sum_p
+    exp(lse_p)`` and ``o = sum_p exp(lse_p - lse) o_p``.  With ``l_p`` the
+    softmax denominator of piece ``p`` and ``m`` any shift, ``exp(lse_p) =
+    l_p`` and the softmax over the union has denominator ``sum_p l_p``, so
+    each piece's normalised output is re-weighted by its share of it.
+    ``o_pieces [P, ..., d]``, ``lse_pieces [P, ...]``; a row with every
+    ``lse_p = -inf`` has ``o = 0`` and ``lse = -inf``.
+    """
+    o_pieces = np.asarray(o_pieces, np.float64)
+    lse_pieces = np.asarray(lse_pieces, np.float64)
+    m = lse_pieces.max(axis=0)
+    empty = ~np.isfinite(m)
+    m_safe = np.where(empty, 0.0, m)
+    w = np.where(np.isfinite(lse_pieces), np.exp(lse_pieces - m_safe), 0.0)
+    total = w.sum(axis=0)
+    total_safe = np.where(empty, 1.0, total)
+    o = (w[..., None] * o_pieces).sum(axis=0) / total_safe[..., None]
+    o = np.where(empty[..., None], 0.0, o)
+    lse = np.where(empty, -math.inf, m_safe + np.log(total_safe))
+    return o, lse
+
+
 # ---------------------------------------------------------------------------
 # the absorbed quantities, by their definitions
 # ---------------------------------------------------------------------------

@@ -267,3 +267,30 @@ def test_strided_tensor_refused():
         m._ptr(t)
     x = torch.zeros(4, 8)
     assert m._ptr(x) == x.data_ptr()
+
+
+def test_block_range_and_combine_validation():
+    """mla_decode_blocks refuses a negative or reversed block range and the
+    shapes only the CUDA-core path takes; mla_combine_pieces refuses P < 1,
+    missing or misaligned pointers and non-tensor-core shapes.  All of it is
+    decided on the host, before anything is launched."""
+    lib = m.raw_lib()
+    d = ctypes.byref(_dims())
+    ok = ctypes.c_void_p(1 << 20)
+
+    def blocks(first, end, dims=d, B=2):
+        return lib.mla_decode_blocks(ok, ok, ok, 4, ok, 4, ok, 64, B, 1, first, end, dims, ok,
+                                     ok, ok, 1 << 40, None)
+
+    assert blocks(-1, 3) == m.MLA_ERR_INVALID_ARG
+    assert blocks(3, 2) == m.MLA_ERR_INVALID_ARG
+    assert blocks(0, 3, B=0) == m.MLA_OK  # nothing to do
+    fp32 = ctypes.byref(m.Dims(H=4, d_h=16, d_c=16, d_r=8, block_size=32, dtype=m.MLA_FP32))
+    assert blocks(0, 3, dims=fp32) == m.MLA_ERR_UNSUPPORTED  # CUDA-core shapes
+    assert lib.mla_combine_pieces(ok, ok, 0, 2, 1, d, ok, ok, None) == m.MLA_ERR_INVALID_ARG
+    assert lib.mla_combine_pieces(None, ok, 2, 2, 1, d, ok, ok, None) == m.MLA_ERR_INVALID_ARG
+    assert lib.mla_combine_pieces(ctypes.c_void_p((1 << 20) + 2), ok, 2, 2, 1, d, ok, ok,
+                                  None) == m.MLA_ERR_INVALID_ARG
+    assert lib.mla_combine_pieces(ok, ok, 2, 2, 1, fp32, ok, ok, None) == \
+        m.MLA_ERR_UNSUPPORTED
+    assert lib.mla_combine_pieces(ok, ok, 2, 0, 1, d, ok, ok, None) == m.MLA_OK

@@ -7,7 +7,11 @@
 * textbook single-head attention (H=1, W_UK = W_UV = I) against PyTorch's
   scaled-dot-product attention in fp64, with and without the RoPE part,
 * one visible token, identical keys, empty rows,
-* block-table permutation invariance, causal query slots, append placement.
+* block-table permutation invariance, causal query slots, append placement,
+* block-range pieces: merged by the log-sum-exp combine they equal the
+  whole decode; a range over every block is the decode; one block against
+  the brute-force softmax over its keys; the combine's weights on a case
+  with known denominators.
 """
 
 import math
@@ -186,3 +190,119 @@ def test_append_places_rows():
         for slot in range(bs):
             if (blk, slot) not in touched:
                 assert np.array_equal(new[blk, slot], cache[blk, slot])
+
+
+# ---- block-range pieces and their merge ------------------------------------
+
+
+def _blocks(case, first, end):
+    return mla.mla_decode_blocks(case["q_nope"], case["q_rope"], case["cache"],
+                                 case["block_table"], case["seqlens"], case["W_UK"],
+                                 case["W_UV"], case["Hq"], first, end)
+
+
+@pytest.mark.parametrize("cuts", [(1,), (2,), (1, 3), (0, 1, 2, 3)])
+@pytest.mark.parametrize("Hq", [1, 2])
+def test_block_pieces_merge_to_the_whole_decode(cuts, Hq):
+    # the softmax over a union of disjoint key sets: each piece's normalised
+    # output re-weighted by its share of the denominator gives the whole row
+    rng = np.random.default_rng(11 + Hq)
+    case = _rand_case(rng, seqlens=(9, 1, 13, 16), Hq=Hq)
+    bounds = (0,) + cuts + (10**6,)
+    pieces = [_blocks(case, a, b) for a, b in zip(bounds, bounds[1:])]
+    out, o_lat, lse = _decode(case)
+    o_m, lse_m = mla.combine_pieces(np.stack([p[1] for p in pieces]),
+                                    np.stack([p[2] for p in pieces]))
+    out_m, _ = mla.combine_pieces(np.stack([p[0] for p in pieces]),
+                                  np.stack([p[2] for p in pieces]))
+    np.testing.assert_allclose(o_m, o_lat, atol=1e-12)
+    np.testing.assert_allclose(out_m, out, atol=1e-12)
+    np.testing.assert_array_equal(np.isfinite(lse_m), np.isfinite(lse))
+    fin = np.isfinite(lse)
+    np.testing.assert_allclose(lse_m[fin], lse[fin], atol=1e-12)
+
+
+def test_block_range_cases():
+    rng = np.random.default_rng(5)
+    case = _rand_case(rng, seqlens=(9, 1, 13))
+    out, o_lat, lse = _decode(case)
+    # a range over every block is the decode itself
+    _, o_all, lse_all = _blocks(case, 0, 10**6)
+    np.testing.assert_array_equal(o_all, o_lat)
+    np.testing.assert_array_equal(lse_all, lse)
+    # a range past every sequence: nothing visible
+    _, o_none, lse_none = _blocks(case, 100, 200)
+    assert np.all(o_none == 0) and np.all(lse_none == -math.inf)
+    # one block: exactly the softmax over that block's keys (brute force)
+    bs = case["cache"].shape[1]
+    _, o_1, lse_1 = _blocks(case, 1, 2)
+    b, h = 2, 1  # sequence of 13 tokens: block 1 holds positions 4..7
+    rows = np.stack([case["cache"][case["block_table"][b, 1], j] for j in range(bs)])
+    d_c = case["W_UK"].shape[2]
+    K = rows[:, :d_c] @ case["W_UK"][h].T
+    s = (K @ case["q_nope"][b, 0, h] + rows[:, d_c:] @ case["q_rope"][b, 0, h]) / math.sqrt(
+        case["W_UK"].shape[1] + case["q_rope"].shape[3])
+    p = np.exp(s - s.max()) / np.exp(s - s.max()).sum()
+    np.testing.assert_allclose(o_1[b, 0, h], p @ rows[:, :d_c], atol=1e-12)
+    assert lse_1[b, 0, h] == pytest.approx(s.max() + math.log(np.exp(s - s.max()).sum()),
+                                           abs=1e-12)
+
+
+def test_combine_weights_and_empty_pieces():
+    # two pieces with known denominators: weights e^{lse_p} / sum
+    o = np.array([[[1.0, 0.0]], [[0.0, 1.0]]])  # [P=2, rows=1, d=2]
+    lse = np.array([[math.log(1.0)], [math.log(3.0)]])
+    om, lm = mla.combine_pieces(o, lse)
+    np.testing.assert_allclose(om[0], [0.25, 0.75], atol=1e-15)
+    assert lm[0] == pytest.approx(math.log(4.0), abs=1e-15)
+    # an empty piece (lse = -inf) weighs nothing; all empty -> 0 / -inf
+    om, lm = mla.combine_pieces(np.array([[[5.0, 7.0]], [[9.0, 9.0]]]),
+                                np.array([[0.5], [-math.inf]]))
+    np.testing.assert_allclose(om[0], [5.0, 7.0])
+    assert lm[0] == pytest.approx(0.5)
+    om, lm = mla.combine_pieces(np.ones((3, 1, 2)), np.full((3, 1), -math.inf))
+    assert np.all(om == 0) and lm[0] == -math.inf
+
+
+def _merge_matches_whole(case, cuts=(1, 3)):
+    bounds = (0,) + cuts + (10**6,)
+    pieces = [_blocks(case, a, b) for a, b in zip(bounds, bounds[1:])]
+    _, o_lat, lse = _decode(case)
+    o_m, lse_m = mla.combine_pieces(np.stack([p[1] for p in pieces]),
+                                    np.stack([p[2] for p in pieces]))
+    fin = np.isfinite(lse)
+    return (np.allclose(o_m, o_lat, atol=1e-9) and np.array_equal(np.isfinite(lse_m), fin)
+            and np.allclose(lse_m[fin], lse[fin], atol=1e-9))
+
+
+def _combine_unweighted(o_pieces, lse_pieces):  # plain mean of the pieces
+    o, lse = _ORIG_COMBINE(o_pieces, lse_pieces)
+    fin = np.isfinite(np.asarray(lse_pieces))
+    return (np.asarray(o_pieces) * fin[..., None]).sum(0) / np.maximum(fin.sum(0), 1)[..., None], lse
+
+
+def _combine_lse_max_only(o_pieces, lse_pieces):  # lse = max_p lse_p
+    o, _ = _ORIG_COMBINE(o_pieces, lse_pieces)
+    return o, np.asarray(lse_pieces).max(axis=0)
+
+
+def _blocks_off_by_one(q_nope, q_rope, cache, block_table, seqlens, W_UK, W_UV, Hq, first,
+                       end, **kw):  # the range ends one block late
+    return _ORIG_BLOCKS(q_nope, q_rope, cache, block_table, seqlens, W_UK, W_UV, Hq, first,
+                        end + 1, **kw)
+
+
+_ORIG_COMBINE = mla.combine_pieces
+_ORIG_BLOCKS = mla.mla_decode_blocks
+
+
+@pytest.mark.parametrize("name,attr,fn", [
+    ("unweighted mean", "combine_pieces", _combine_unweighted),
+    ("lse is the max", "combine_pieces", _combine_lse_max_only),
+    ("range one block long", "mla_decode_blocks", _blocks_off_by_one),
+])
+def test_planted_piece_mistakes_are_caught(name, attr, fn, monkeypatch):
+    case = _rand_case(np.random.default_rng(3), seqlens=(9, 1, 13, 16))
+    assert _merge_matches_whole(case)
+    monkeypatch.setattr(mla, attr, fn)
+    assert not _merge_matches_whole(case), f"'{name}' slipped past the merge invariant"
