@@ -768,9 +768,12 @@ __global__ void __launch_bounds__(kRThreads, 1)
             uint32_t pk[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) pk[e] = ptx::pack_bf16x2(v[i][2 * e], v[i][2 * e + 1]);
-            uint4 *d4 = reinterpret_cast<uint4 *>(dst + half * 128 + i * 16);
-            d4[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            d4[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+            // 32 bytes per lane in one store (the row base is 32-byte aligned)
+            asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(
+                             dst + half * 128 + i * 16),
+                         "r"(pk[0]), "r"(pk[1]), "r"(pk[2]), "r"(pk[3]), "r"(pk[4]), "r"(pk[5]),
+                         "r"(pk[6]), "r"(pk[7])
+                         : "memory");
           }
         }
       }
