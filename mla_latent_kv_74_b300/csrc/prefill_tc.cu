@@ -143,7 +143,7 @@ __device__ __forceinline__ bool wait_warp(uint64_t *bar, uint32_t parity, volati
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_q,   // q_nope [total][H*128]
                         const __grid_constant__ CUtensorMap tm_qr,  // q_rope [total][H*64]
-                        const __grid_constant__ CUtensorMap tm_kv,  // [K_nope | V] [total][H*256]
+                        const __grid_constant__ CUtensorMap tm_kv,  // [K_nope | V] [H*4][total][64]
                         const __grid_constant__ CUtensorMap tm_kr,  // k_R [total][64]
                         PrefillArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -253,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tma_load_2d(qd + kBox, &tm_q, qb, it.h * kDh + 64, it.tok0 + it.q0);
         ptx::tma_load_2d(qd + 2 * kBox, &tm_qr, qb, it.h * kDr, it.tok0 + it.q0);
         ++f;
-        const int xk = it.h * 2 * kDh;
+        const int zk = it.h * 4;  // the head's K_nope chunks
         for (int j = 0; j < it.n; ++j, ++f) {
           if (!fill_wait(f)) {
             ok = false;
@@ -263,8 +263,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint64_t *kb = &bars->k_full[f % kKStages];
           const int y = it.tok0 + j * kKT;
           ptx::mbar_arrive_expect_tx(kb, kKStage);
-          ptx::tma_load_2d(kd, &tm_kv, kb, xk, y);
-          ptx::tma_load_2d(kd + kBox, &tm_kv, kb, xk + 64, y);
+          ptx::tma_load_3d(kd, &tm_kv, kb, 0, y, zk);
+          ptx::tma_load_3d(kd + kBox, &tm_kv, kb, 0, y, zk + 1);
           ptx::tma_load_2d(kd + 2 * kBox, &tm_kr, kb, 0, y);
         }
       }
@@ -285,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         if (it.n == 0) break;
-        const int xv = it.h * 2 * kDh + kDh;
+        const int zv = it.h * 4 + 2;  // the head's V chunks
         for (int j = 0; j < it.n; ++j, ++fv) {
           const int st = fv % kVStages;
           if (fv >= kVStages &&
@@ -295,8 +295,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           uint8_t *vd = smem + kOffV + st * kVStage;
           ptx::mbar_arrive_expect_tx(&bars->v_full[st], kVStage);
-          ptx::tma_load_2d(vd, &tm_kv, &bars->v_full[st], xv, it.tok0 + j * kKT);
-          ptx::tma_load_2d(vd + kBox, &tm_kv, &bars->v_full[st], xv + 64, it.tok0 + j * kKT);
+          ptx::tma_load_3d(vd, &tm_kv, &bars->v_full[st], 0, it.tok0 + j * kKT, zv);
+          ptx::tma_load_3d(vd + kBox, &tm_kv, &bars->v_full[st], 0, it.tok0 + j * kKT, zv + 1);
         }
       }
       if (!ok) set_fail();
@@ -603,16 +603,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---- keys and values rebuilt from the latents ----
 //
-// kv[t, h, 0:128] = W_UK[h] c_t and kv[t, h, 128:256] = W_UV[h] c_t for a
-// tile of 128 tokens and kRebuildHeads consecutive heads per CTA:
+// [W_UK[h] c_t ; W_UV[h] c_t] (256 columns, stored as four 64-column chunks
+// kv[h][c][t][64], token-minor) for a tile of 128 tokens and kRebuildHeads
+// consecutive heads per CTA:
 //   D[t][n] = sum_c C[t][c] W[n][c]   M = 128 tokens, N = 256 (W_UK[h] rows
 //   then W_UV[h] rows), K = d_c = 512
 // The latent tile (128 x 512, 128 KB) is loaded once and stays in shared
 // memory; the weights stream through a ring of 64-wide K chunks (W_UK and
 // W_UV boxes side by side: one 256-row K-major operand).  Two TMEM
 // accumulators (256 columns each) let the epilogue of one head overlap the
-// MMAs of the next.  Thread = token row = TMEM lane, so each thread writes
-// its token's 512 contiguous bytes of the head.
+// MMAs of the next.  Thread = token row = TMEM lane: each thread writes its
+// token's 128-byte row of each chunk, and a warp's 32 consecutive tokens
+// fill 4 KB of contiguous memory.
 constexpr int kRebuildHeads = 8;
 constexpr int kRStages = 3;
 constexpr uint32_t kRBoxA = 128 * 128;       // 128 tokens x 64 latents
@@ -634,7 +636,7 @@ static_assert(kRSmemBytes <= 232448, "over the 227 KB shared-memory limit");
 
 struct RebuildArgs {
   int T, H;
-  __nv_bfloat16 *kv;  // [T][H][256]
+  __nv_bfloat16 *kv;  // [H][4][T][64]: 64-column chunks of [K_nope | V], token-minor
   int *err;
   unsigned long long *next_item;  // the attention kernel's work-list counter, zeroed here
 };
@@ -754,7 +756,10 @@ __global__ void __launch_bounds__(kRThreads, 1)
         break;
       }
       ptx::tc_fence_after();
-      __nv_bfloat16 *dst = a.kv + ((size_t)(store ? t0 + row : 0) * a.H + h0 + g) * 256;
+      // the 64-column chunk c (0-1 K_nope, 2-3 V) of head h0 + g for token t
+      // lives at kv[((h0 + g) * 4 + c) * T + t][64]: a warp's 32 consecutive
+      // tokens fill 4 KB of contiguous rows
+      __nv_bfloat16 *dst = a.kv + ((size_t)(h0 + g) * 4 * a.T + (store ? t0 + row : 0)) * 64;
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         float v[8][16];
@@ -768,9 +773,9 @@ __global__ void __launch_bounds__(kRThreads, 1)
             uint32_t pk[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) pk[e] = ptx::pack_bf16x2(v[i][2 * e], v[i][2 * e + 1]);
-            // 32 bytes per lane in one store (the row base is 32-byte aligned)
+            // 32 bytes per lane in one store (chunk rows are 128-byte aligned)
             asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(
-                             dst + half * 128 + i * 16),
+                             dst + (size_t)(2 * half + (i >> 2)) * a.T * 64 + (i & 3) * 16),
                          "r"(pk[0]), "r"(pk[1]), "r"(pk[2]), "r"(pk[3]), "r"(pk[4]), "r"(pk[5]),
                          "r"(pk[6]), "r"(pk[7])
                          : "memory");
@@ -847,8 +852,10 @@ cudaError_t launch_prefill_tc(const void *q_nope, const void *q_rope, const void
                          CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_tmap_2d_bf16(&tm_qr, q_rope, H * kDr, total, H * kDr * 2, 64, kQT,
                          CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_tmap_2d_bf16(&tm_kv, kv, H * 2 * kDh, total, H * 2 * kDh * 2, 64, kKT,
-                         CU_TENSOR_MAP_SWIZZLE_128B) ||
+      // [K_nope | V] as [H * 4 chunks][total][64]: boxes of 128 tokens x 64
+      // columns, the same shared-memory tiles as a row-major view would give
+      !make_tmap_3d(&tm_kv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, kv, 64, total, (uint64_t)H * 4,
+                    128, (uint64_t)total * 128, 64, kKT, 1, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_tmap_2d_bf16(&tm_kr, k_r, kDr, total, kDr * 2, 64, kKT, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   e = cudaFuncSetAttribute(prefill_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
