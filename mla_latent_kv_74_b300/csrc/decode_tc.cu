@@ -213,7 +213,9 @@ __device__ __forceinline__ void trace_ev(int pair, int npairs, uint32_t rank, in
   if (slot >= 0 && g >= 0 && g < kTraceTiles) g_trace[slot][rank][ev][g] = ptx::globaltimer_ns();
 }
 #define MLA_TRACE_EV(ev, g) trace_ev(pair, a.npairs, rank, (ev), (g))
+#define SH_TRACE_EV(side, ev, g) trace_ev(cta, a.npairs, (side), (ev), (g))
 #else
+#define SH_TRACE_EV(side, ev, g) ((void)0)
 #define MLA_TRACE_EV(ev, g) ((void)0)
 #define MLA_TRACE_CTA(k) ((void)0)
 #endif
@@ -1134,6 +1136,556 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (warp == 1) ptx::tmem_dealloc(tmem, 512);
 }
 
+// ---------------------------------------------------------------------------
+// Few heads (H <= 16, the DeepSeek-V2-Lite shape): one CTA per SM, no pair.
+//
+// The pair exists because O (128 rows x 512 fp32 columns) and the query do
+// not fit one SM's TMEM together.  With at most 16 heads O fits once it is
+// kept transposed: O^T = C^T P^T with M = 128 latent columns per MMA (four
+// MMAs cover d_c = 512), N = 16 head columns and K = 64 tokens, so O^T takes
+// 4 x 16 TMEM columns next to the query (288) and two 64-column score
+// buffers.  Every SM then streams its own range of tiles from HBM; nothing
+// crosses DSMEM.  The scores are computed as in the pair kernel (S = Q C^T,
+// M = 128 rows of which the first H are heads, N = 64 tokens, A = query in
+// TMEM); P (16 rows x 64 tokens, bf16) goes to shared memory as the K-major
+// B operand of the PV MMAs, whose A operand is the same ring stage read
+// MN-major (latent contiguous).  The plan, the pieces and the combine are
+// the pair kernel's, with one CTA in the place of a pair.
+//
+// Warp roles (288 threads): warp 0 TMA producer; warps 1 and 2 QK^T issuers
+// (even / odd tiles); warp 3 TMEM owner and PV issuer; warps 4-7 rescale
+// O^T and run the segment epilogues (TMEM lanes 32*(w%4)...); warp 8 the
+// online softmax, one head row per lane (TMEM lanes 0-31).
+namespace sh {
+constexpr int kThreads = 288;
+constexpr int kRows = 16;                          // head rows (H <= 16)
+constexpr uint32_t kQBox = kRows * 128;            // 16 rows x 128 B
+constexpr uint32_t kQBytes = 9 * kQBox;            // one item's [q_lat ; q_rope]
+constexpr uint32_t kOffP = kStages * kSStage;      // two P buffers
+constexpr uint32_t kPBytes = kRows * 128;          // 16 rows x 64 bf16
+constexpr uint32_t kOffAux = kOffP + 2 * kPBytes;  // per P buffer: alpha[16], flag
+constexpr uint32_t kAuxBytes = 80;
+constexpr uint32_t kOffStats = kOffAux + 2 * kAuxBytes;  // m[16], l[16]
+constexpr uint32_t kOffBars = kOffStats + 2 * kRows * 4;
+struct Bars {
+  uint64_t full[6], empty[kStages], qfull[2];
+  uint64_t q_full, q_free, s_full[2], s_free[2], p_full[2], p_free[2];
+  uint64_t pv_done, ev_full, ev_done, o_full, stats_full, stats_free, drain[3];
+};
+constexpr uint32_t kOffMisc = kOffBars + ((sizeof(Bars) + 15) / 16) * 16;
+constexpr uint32_t kSmemBytes = kOffMisc + ((sizeof(Misc) + 15) / 16) * 16;
+static_assert(kSmemBytes <= 232448, "over the 227 KB shared-memory limit");
+static_assert(kOffP % 1024 == 0, "P buffers must be 1024-byte aligned");
+static_assert(kQBytes <= kSStage, "an item's query fits one ring stage");
+// TMEM columns: query 0-287, score buffers 320 + 64 b, O^T chunk q at 448 + 16 q
+constexpr uint32_t kTmemQ = 0, kTmemS = 320, kTmemO = 448;
+}  // namespace sh
+
+__global__ void __launch_bounds__(sh::kThreads, 1)
+    decode_sh_kernel(const __grid_constant__ CUtensorMap tm_cache,
+                     const __grid_constant__ CUtensorMap tm_qlat,
+                     const __grid_constant__ CUtensorMap tm_qrope, DecodeArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  sh::Bars *bars = reinterpret_cast<sh::Bars *>(smem + sh::kOffBars);
+  Misc *misc = reinterpret_cast<Misc *>(smem + sh::kOffMisc);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int cta = blockIdx.x;
+  const int W = a.B * a.Hq;
+  volatile int *abort = &misc->abort;
+  MLA_TRACE_CTA(0);
+
+  // ---- setup: barriers, TMEM, this CTA's tile range ----
+  if (threadIdx.x == 0) {
+    misc->abort = 0;
+    misc->ev_type = 0;
+    misc->bad_smem = (ptx::smem_u32(smem) & 1023u) != 0;
+    for (int s = 0; s < 6; ++s) ptx::mbar_init(&bars->full[s], 1);
+    for (int s = 0; s < kStages; ++s) ptx::mbar_init(&bars->empty[s], 1);
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(&bars->qfull[i], 1);
+      ptx::mbar_init(&bars->s_full[i], 1);
+      ptx::mbar_init(&bars->s_free[i], 32);
+      ptx::mbar_init(&bars->p_full[i], 32);
+      ptx::mbar_init(&bars->p_free[i], 1);
+    }
+    ptx::mbar_init(&bars->q_full, 32);
+    ptx::mbar_init(&bars->q_free, 2);
+    ptx::mbar_init(&bars->pv_done, 1);
+    ptx::mbar_init(&bars->ev_full, 1);
+    ptx::mbar_init(&bars->ev_done, 128);
+    ptx::mbar_init(&bars->o_full, 1);
+    ptx::mbar_init(&bars->stats_full, 32);
+    ptx::mbar_init(&bars->stats_free, 128);
+    for (int i = 0; i < 3; ++i) ptx::mbar_init(&bars->drain[i], 1);
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::tma_prefetch_desc(&tm_cache);
+    ptx::tma_prefetch_desc(&tm_qlat);
+    ptx::tma_prefetch_desc(&tm_qrope);
+  }
+  if (warp == 3) ptx::tmem_alloc(&misc->tmem, 512);
+  ptx::grid_dependency_wait();
+  ptx::launch_dependents();
+  {
+    // tiles per item -> scan (scratch in the ring) -> this CTA's range
+    int *pre = reinterpret_cast<int *>(smem);
+    bool any_bad = false;
+    for (int u = threadIdx.x; u < W; u += blockDim.x) {
+      bool bad = false;
+      const int n = visible_len(a, u, &bad);
+      any_bad |= bad;
+      const int nt = (n + kTile - 1) / kTile;
+      pre[u + 1] = nt > 0 ? nt + kItemCost : 0;
+    }
+    if (any_bad && cta == 0) set_device_error(a.err, kDevBounds);
+    __syncthreads();
+    if (warp == 0) {
+      int running = 0;
+      for (int base = 0; base < W; base += 32) {
+        const int idx = base + lane;
+        int v = idx < W ? pre[idx + 1] : 0;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const int u = __shfl_up_sync(0xffffffffu, v, off);
+          if (lane >= off) v += u;
+        }
+        if (idx < W) pre[idx + 1] = running + v;
+        running += __shfl_sync(0xffffffffu, v, 31);
+      }
+      if (lane == 0) pre[0] = 0;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      const int t_total = pre[W];
+      const int per = (t_total + a.npairs - 1) / a.npairs;
+      const int tb = min(t_total, cta * per);
+      const int te = min(t_total, tb + per);
+      int lo = 0, hi = W;  // first item whose tile range ends after tb
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (pre[mid + 1] <= tb) lo = mid + 1;
+        else hi = mid;
+      }
+      misc->t_begin = tb;
+      misc->t_end = te;
+      misc->w0 = lo;
+      misc->s0 = lo < W ? pre[lo] : t_total;
+      misc->t_total = t_total;
+      if (cta == 0) a.plan[0] = per;
+    }
+    if (cta == 0)  // the plan of the combine kernel
+      for (int w = threadIdx.x; w <= W; w += blockDim.x) a.plan[1 + w] = pre[w];
+  }
+  ptx::tc_fence_before();
+  __syncthreads();  // the scratch is the ring: read before the first load
+  ptx::tc_fence_after();
+  const uint32_t tmem = misc->tmem;
+  const bool bad_smem = misc->bad_smem != 0;
+  const int t_begin = misc->t_begin, t_end = misc->t_end, w0 = misc->w0, s0 = misc->s0;
+  MLA_TRACE_CTA(1);
+  SegIter<false> it;
+  it.init(&a, W, t_begin, t_end, w0, s0);
+  int item, lt0, lt1, n_vis;
+  bool whole;
+
+  if (bad_smem) {
+    if (threadIdx.x == 0) set_device_error(a.err, kDevTimeout);
+  } else if (warp == 0) {
+    // ===================== TMA producer =====================
+    // ring position r: one stage for each segment's query, then its tiles
+    int g = 0, r = 0, seg = 0;
+    bool failed = false;
+    TableWindow cur;
+    while (!failed && !*abort && it.next(&item, &lt0, &lt1, &whole, &n_vis)) {
+      const int b = item / a.Hq;
+      cur.reset(a.block_table + (size_t)b * a.max_blocks, lt1);
+      {
+        const int st = r % kStages;
+        if (r >= kStages && !wait_bar_warp(&bars->empty[st], ((r / kStages) - 1) & 1, abort)) {
+          failed = true;
+          break;
+        }
+        if (lane == 0) {
+          uint8_t *dst = smem + st * kSStage;
+          uint64_t *qb = &bars->qfull[seg & 1];
+          ptx::mbar_arrive_expect_tx(qb, sh::kQBytes);
+          ptx::tma_load_3d(dst, &tm_qlat, qb, 0, item * a.H, 0);  // 8 latent boxes
+          ptx::tma_load_2d(dst + 8 * sh::kQBox, &tm_qrope, qb, 0, item * a.H);
+        }
+        ++r;
+      }
+      for (int lt = lt0; lt < lt1; ++lt, ++g, ++r) {
+        const int st = r % kStages;
+        if (r >= kStages && !wait_bar_warp(&bars->empty[st], ((r / kStages) - 1) & 1, abort)) {
+          failed = true;
+          break;
+        }
+        int blk = cur.at(lt, lane);
+        if (blk < 0 || blk >= a.num_blocks) blk = 0;  // reported by the softmax warp
+        if (lane == 0) {
+          SH_TRACE_EV(1, 8, g);
+          uint64_t *fb = &bars->full[g % 6];
+          ptx::mbar_arrive_expect_tx(fb, 9 * kBox);
+          ptx::tma_load_3d(smem + st * kSStage, &tm_cache, fb, 0, blk * kTile, 0);
+        }
+      }
+      ++seg;
+    }
+    if (failed) atomicExch(&misc->abort, 1);
+    // leave only after every stage this CTA filled was released
+    if (!*abort)
+      for (int k = r - kStages < 0 ? 0 : r - kStages; k < r; ++k)
+        wait_bar_warp(&bars->empty[k % kStages], (k / kStages) & 1, abort);
+  } else if (warp == 1 || warp == 2) {
+    // ========== QK^T issuers: warp 1 even tiles, warp 6 odd ==========
+    if (lane == 0) {
+      const int mine = warp - 1;
+      const uint32_t idesc = ptx::idesc_bf16(128, kTile, false, false);
+      const uint64_t ring_desc = ptx::smem_desc(ptx::smem_u32(smem), 16, 1024, ptx::kSw128);
+      int g = 0, r = 0, seg = 0;
+      bool failed = false;
+      while (!failed && it.next(&item, &lt0, &lt1, &whole, &n_vis)) {
+        if (!wait_bar(&bars->q_full, seg & 1, abort)) { failed = true; break; }
+        ptx::tc_fence_after();
+        ++r;  // the segment's query stage
+        for (int lt = lt0; lt < lt1; ++lt, ++g, ++r) {
+          if ((g & 1) != mine) continue;
+          const int st = r % kStages, sb = g & 1;
+          if (!wait_bar(&bars->full[g % 6], (g / 6) & 1, abort)) { failed = true; break; }
+          SH_TRACE_EV(1, 1, g);
+          // buffer sb last held tile g-2, read by the softmax warp
+          if (g >= 2 && !wait_bar(&bars->s_free[sb], ((g - 2) >> 1) & 1, abort)) {
+            failed = true;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t d = tmem + sh::kTmemS + sb * kTile;
+          const uint64_t bs = ring_desc + (uint64_t)((st * kSStage) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < 36; ++kk)  // 9 boxes (8 latent + RoPE) x 4 k-steps of 16
+            ptx::mma_bf16_ts(d, tmem + sh::kTmemQ + kk * 8,
+                             bs + (uint64_t)((((kk >> 2) * kBox) + (kk & 3) * 32) >> 4), idesc,
+                             kk != 0);
+          ptx::mma_commit(&bars->s_full[sb]);
+          SH_TRACE_EV(1, 2, g);
+        }
+        if (failed) break;
+        ptx::mma_commit(&bars->q_free);
+        ++seg;
+      }
+      uint64_t *dr = &bars->drain[mine];
+      ptx::mma_commit(dr);
+      ptx::mbar_wait(dr, 0);
+      if (failed) atomicExch(&misc->abort, 1);
+    }
+  } else if (warp == 3) {
+    // ===================== PV issuer: O^T += C^T P^T =====================
+    if (lane == 0) {
+      const uint32_t idesc = ptx::idesc_bf16(128, sh::kRows, true, false);
+      // A: the stage's latent boxes MN-major (64 latent columns per 128-byte
+      // row, boxes 8 KB apart, 8 tokens per 1 KB); B: P, K-major
+      const uint64_t ring_desc = ptx::smem_desc(ptx::smem_u32(smem), kBox, 1024, ptx::kSw128);
+      const uint64_t p_desc =
+          ptx::smem_desc(ptx::smem_u32(smem + sh::kOffP), 16, 1024, ptx::kSw128);
+      const uint8_t *aux = smem + sh::kOffAux;
+      int g = 0, r = 0, seg = 0, nev = 0, npv = 0;
+      bool failed = false;
+      auto post = [&](int type) -> bool {
+        misc->ev_type = type;
+        ptx::mbar_arrive(&bars->ev_full);
+        const bool ok = wait_bar(&bars->ev_done, nev & 1, abort);
+        ++nev;
+        return ok;
+      };
+      while (!failed && it.next(&item, &lt0, &lt1, &whole, &n_vis)) {
+        ++r;  // the segment's query stage
+        for (int lt = lt0; lt < lt1; ++lt, ++g, ++r) {
+          const int st = r % kStages, pb = g & 1;
+          if (!wait_bar(&bars->full[g % 6], (g / 6) & 1, abort) ||
+              !wait_bar(&bars->p_full[pb], (g >> 1) & 1, abort)) {
+            failed = true;
+            break;
+          }
+          SH_TRACE_EV(0, 1, g);
+          const uint32_t flag =
+              *reinterpret_cast<const volatile uint32_t *>(aux + pb * sh::kAuxBytes + 64);
+          if (lt != lt0 && flag != 0) {
+            // O^T *= alpha (per head column) once every PV so far has accumulated
+            ptx::mma_commit(&bars->pv_done);
+            if (!wait_bar(&bars->pv_done, npv & 1, abort)) { failed = true; break; }
+            ++npv;
+            if (!post(kEvRescale | (pb << 4))) { failed = true; break; }
+          }
+          ptx::tc_fence_after();
+          const uint64_t ad = ring_desc + (uint64_t)((st * kSStage) >> 4);
+          const uint64_t bd = p_desc + (uint64_t)((pb * sh::kPBytes) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk)
+#pragma unroll
+            for (int q = 0; q < kDc / 128; ++q)
+              ptx::mma_bf16(tmem + sh::kTmemO + q * sh::kRows,
+                            ad + (uint64_t)((2 * q * kBox + kk * 2048) >> 4),
+                            bd + (uint64_t)((kk * 32) >> 4), idesc,
+                            (lt == lt0 && kk == 0) ? 0u : 1u);
+          ptx::mma_commit(&bars->p_free[pb]);
+          ptx::mma_commit(&bars->empty[st]);
+          SH_TRACE_EV(0, 3, g);
+        }
+        if (failed) break;
+        ptx::mma_commit(&bars->o_full);
+        if (!wait_bar(&bars->o_full, seg & 1, abort)) { failed = true; break; }
+        SH_TRACE_EV(0, 7, seg);
+        if (!post(kEvEpilogue)) { failed = true; break; }
+        SH_TRACE_EV(0, 7, 128 + seg);
+        ++seg;
+      }
+      misc->ev_type = kEvDone;
+      ptx::mbar_arrive(&bars->ev_full);
+      ptx::mma_commit(&bars->drain[2]);
+      ptx::mbar_wait(&bars->drain[2], 0);
+      if (failed) atomicExch(&misc->abort, 1);
+    }
+  } else if (warp >= 4 && warp <= 7) {
+    // ============ O^T rescale and segment epilogues ============
+    // lane of TMEM = latent column c within each 128-column chunk
+    const int wq = warp & 3;
+    const int cl = 32 * wq + lane;
+    const uint32_t lane_base = (uint32_t)(32 * wq) << 16;
+    const uint8_t *aux = smem + sh::kOffAux;
+    const float *stats = reinterpret_cast<const float *>(smem + sh::kOffStats);
+    int seg = 0, nev = 0;
+    bool failed = false;
+    for (;;) {
+      if (!wait_bar_warp(&bars->ev_full, nev & 1, abort)) { failed = true; break; }
+      ++nev;
+      const int ev = *reinterpret_cast<volatile int *>(&misc->ev_type);
+      if ((ev & 15) == kEvDone) break;
+      if ((ev & 15) == kEvRescale) {
+        const float *al = reinterpret_cast<const float *>(aux + (ev >> 4) * sh::kAuxBytes);
+        float f[sh::kRows];
+#pragma unroll
+        for (int h = 0; h < sh::kRows; ++h) f[h] = al[h];
+        ptx::tc_fence_after();
+#pragma unroll 1
+        for (int q = 0; q < kDc / 128; ++q) {
+          float v[16];
+          ptx::tmem_ld16(tmem + lane_base + sh::kTmemO + q * sh::kRows, v);
+          ptx::tmem_ld_wait();
+#pragma unroll
+          for (int h = 0; h < 16; ++h) v[h] *= f[h];
+          ptx::tmem_st16(tmem + lane_base + sh::kTmemO + q * sh::kRows, v);
+        }
+        ptx::tmem_st_wait();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(&bars->ev_done);
+        continue;
+      }
+      // epilogue of the next segment (its PVs are complete)
+      if (!it.next(&item, &lt0, &lt1, &whole, &n_vis)) { failed = true; break; }
+      if (!wait_bar_warp(&bars->stats_full, seg & 1, abort)) { failed = true; break; }
+      ptx::tc_fence_after();
+      float inv_l[sh::kRows];
+      bool seg_bad = false;
+#pragma unroll
+      for (int h = 0; h < sh::kRows; ++h) {
+        const float l = stats[sh::kRows + h];
+        seg_bad |= l < 0.f;
+        inv_l[h] = l > 0.f ? 1.f / l : 0.f;
+      }
+      const float m_me = stats[lane & 15], l_me = stats[sh::kRows + (lane & 15)];
+      ptx::mbar_arrive(&bars->stats_free);
+      if (seg_bad) {
+#pragma unroll
+        for (int h = 0; h < sh::kRows; ++h) inv_l[h] = 0.f;
+      }
+      const int slot_idx = 2 * cta + ((lt0 == 0) ? 1 : 0);  // partial slot
+      __nv_bfloat16 *dst = whole ? a.o_lat + (size_t)item * a.H * kDc
+                                 : a.o_part + (size_t)slot_idx * 128 * kDc;
+#pragma unroll 1
+      for (int q = 0; q < kDc / 128; ++q) {
+        float v[16];
+        ptx::tmem_ld16(tmem + lane_base + sh::kTmemO + q * sh::kRows, v);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int h = 0; h < sh::kRows; ++h)
+          if (h < a.H) dst[(size_t)h * kDc + q * 128 + cl] = __float2bfloat16_rn(v[h] * inv_l[h]);
+      }
+      if (wq == 0 && lane < a.H) {
+        const float lse_val = l_me > 0.f ? (m_me + log2f(l_me)) * kLn2 : -INFINITY;
+        if (whole)
+          a.lse[(size_t)item * a.H + lane] = seg_bad ? -INFINITY : lse_val;
+        else  // NaN poisons the item in the combine
+          a.lse_part[(size_t)slot_idx * 128 + lane] = seg_bad ? __int_as_float(0x7fc00000) : lse_val;
+      }
+      if (seg_bad && wq == 0 && lane == 0) set_device_error(a.err, kDevBounds);
+      __syncwarp();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&bars->ev_done);
+      ++seg;
+    }
+    if (failed) atomicExch(&misc->abort, 1);
+  } else if (warp == 8) {
+    // ============ online softmax: lane = head row (TMEM lanes 0-31) ============
+    const int row = lane;
+    const bool real = row < a.H;
+    const float c = a.scale_log2;
+    float *stats = reinterpret_cast<float *>(smem + sh::kOffStats);
+    uint8_t *aux = smem + sh::kOffAux;
+    int g = 0, r = 0, seg = 0;
+    bool failed = false;
+    while (!failed && it.next(&item, &lt0, &lt1, &whole, &n_vis)) {
+      const int b = item / a.Hq;
+      bool seg_bad;
+      {  // block-table entries this segment reads
+        const int32_t *tbl = a.block_table + (size_t)b * a.max_blocks;
+        bool bad = false;
+        for (int lt = lt0 + lane; lt < lt1; lt += 32) {
+          const int blk = tbl[lt];
+          bad |= (blk < 0 || blk >= a.num_blocks);
+        }
+        seg_bad = __any_sync(0xffffffffu, bad);
+      }
+      // -- the item's query -> TMEM, once the previous segment's QK^T is done --
+      const int rq = r;
+      r += 1 + (lt1 - lt0);
+      if (seg > 0 && !wait_bar_warp(&bars->q_free, (seg - 1) & 1, abort)) { failed = true; break; }
+      if (!wait_bar_warp(&bars->qfull[seg & 1], (seg >> 1) & 1, abort)) { failed = true; break; }
+      ptx::tc_fence_after();
+      {
+        // box k holds columns 64k..64k+63 of the 16 rows as 128-byte rows,
+        // 16-byte chunk c of row h at (c ^ h%8)
+        const uint8_t *qrow = smem + (rq % kStages) * kSStage + (row & 15) * 128;
+#pragma unroll
+        for (int k = 0; k < 9; ++k) {
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t v[16];
+#pragma unroll
+            for (int c2 = 0; c2 < 4; ++c2) {
+              const int cc = 4 * hh + c2;
+              uint4 x = *reinterpret_cast<const uint4 *>(qrow + k * sh::kQBox + ((cc ^ (row & 7)) << 4));
+              if (!real) x = make_uint4(0, 0, 0, 0);
+              v[4 * c2] = x.x;
+              v[4 * c2 + 1] = x.y;
+              v[4 * c2 + 2] = x.z;
+              v[4 * c2 + 3] = x.w;
+            }
+            ptx::tmem_st16_nc(tmem + sh::kTmemQ + k * 32 + hh * 16, v);
+          }
+        }
+      }
+      ptx::tmem_st_wait();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&bars->q_full);
+      if (lane == 0) SH_TRACE_EV(1, 7, seg);
+      __syncwarp();  // every lane has read the stage
+      if (lane == 0) ptx::mbar_arrive(&bars->empty[rq % kStages]);
+
+      float m_run = -INFINITY, l_run = 0.f;
+      for (int lt = lt0; lt < lt1; ++lt, ++g) {
+        const int sb = g & 1;
+        if (!wait_bar_warp(&bars->s_full[sb], (g >> 1) & 1, abort)) { failed = true; break; }
+        if (lane == 0) SH_TRACE_EV(1, 4, g);
+        ptx::tc_fence_after();
+        float s[64];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float v[16];
+          ptx::tmem_ld16(tmem + sh::kTmemS + sb * kTile + q * 16, v);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) s[q * 16 + i] = v[i];
+        }
+        ptx::tmem_ld_wait();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(&bars->s_free[sb]);  // the buffer goes back to tile g+2
+        const int tok0 = lt * kTile;
+        if (tok0 + kTile > n_vis) {
+#pragma unroll
+          for (int j = 0; j < 64; ++j)
+            if (tok0 + j >= n_vis) s[j] = -INFINITY;
+        }
+        float mx4[4] = {s[0], s[1], s[2], s[3]};
+#pragma unroll
+        for (int j = 4; j < 64; ++j) mx4[j & 3] = fmaxf(mx4[j & 3], s[j]);
+        const float mt = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * c;
+        float m_use = mt, alpha = 1.f;
+        bool resc = false;
+        if (lt != lt0) {
+          if (mt > m_run + kRescaleThreshold) {
+            alpha = ptx::ex2(m_run - mt);
+            resc = true;
+          } else {
+            m_use = m_run;
+          }
+        }
+        uint32_t pk[32];
+        float ls[2] = {0.f, 0.f};
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float p0 = ptx::ex2(fmaf(s[2 * i], c, -m_use));
+          const float p1 = ptx::ex2(fmaf(s[2 * i + 1], c, -m_use));
+          ls[i & 1] += p0 + p1;
+          pk[i] = ptx::pack_bf16x2(p0, p1);
+        }
+        l_run = (lt == lt0) ? ls[0] + ls[1] : l_run * alpha + (ls[0] + ls[1]);
+        m_run = m_use;
+        // P buffer sb was last read by the PV of tile g-2
+        if (g >= 2 && !wait_bar_warp(&bars->p_free[sb], ((g - 2) >> 1) & 1, abort)) {
+          failed = true;
+          break;
+        }
+        if (row < sh::kRows) {
+          uint8_t *prow = smem + sh::kOffP + sb * sh::kPBytes + row * 128;
+#pragma unroll
+          for (int cc = 0; cc < 8; ++cc)
+            *reinterpret_cast<uint4 *>(prow + ((cc ^ (row & 7)) << 4)) =
+                real ? make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3])
+                     : make_uint4(0, 0, 0, 0);
+          reinterpret_cast<float *>(aux + sb * sh::kAuxBytes)[row] = real ? alpha : 1.f;
+        }
+        const uint32_t flag = __ballot_sync(0xffffffffu, resc && real);
+        if (lane == 0) *reinterpret_cast<uint32_t *>(aux + sb * sh::kAuxBytes + 64) = flag;
+        ptx::fence_proxy_async_smem();  // P is read by the tensor core (async proxy)
+        ptx::mbar_arrive(&bars->p_full[sb]);
+        if (lane == 0) SH_TRACE_EV(1, 3, g);
+      }
+      if (failed) break;
+      // -- segment end: the row statistics for the epilogue --
+      if (seg > 0 && !wait_bar_warp(&bars->stats_free, (seg - 1) & 1, abort)) { failed = true; break; }
+      if (row < sh::kRows) {
+        stats[row] = m_run;
+        stats[sh::kRows + row] = (seg_bad && real) ? -1.f : l_run;
+      }
+      ptx::mbar_arrive(&bars->stats_full);
+      ++seg;
+    }
+    if (failed) atomicExch(&misc->abort, 1);
+    // items with nothing visible (or an invalid length): o = 0, lse = -inf
+    for (int w = cta; w < W; w += a.npairs) {
+      if (item_tiles(a, w) != 0) continue;
+      if (real) {
+        const size_t rr = (size_t)w * a.H + row;
+        uint4 *d4 = reinterpret_cast<uint4 *>(a.o_lat + rr * kDc);
+        for (int i = 0; i < kDc * 2 / 16; ++i) d4[i] = make_uint4(0, 0, 0, 0);
+        a.lse[rr] = -INFINITY;
+      }
+    }
+  }
+
+  // ---- teardown ----
+  __syncwarp();
+  ptx::tc_fence_before();
+  __syncthreads();
+  MLA_TRACE_CTA(2);
+  if (misc->abort) {
+    if (threadIdx.x == 0) set_device_error(a.err, kDevTimeout);
+    __nanosleep(20000);  // copies issued before the stop have landed
+  }
+  ptx::tc_fence_after();
+  if (warp == 3) ptx::tmem_dealloc(tmem, 512);
+}
+
 // Merge the partial pieces of every item that was cut between pairs
 // (log-sum-exp weights): one warp per output row (item w, head h), eight rows
 // per block.  Lane i weighs piece p0 + i (pieces of one item <= 32 per round),
@@ -1297,10 +1849,11 @@ __global__ void __launch_bounds__(32 * kCombineRows) combine_tc_kernel(DecodeArg
   if (lane == 0) a.lse[rowg] = mx + logf(sum);
 }
 
+// Two piece slots per pair, or per CTA of the few-heads kernel.
 size_t part_bytes() {
-  return align_up((size_t)2 * kMaxPairs * 128 * kDc * sizeof(__nv_bfloat16), 256);
+  return align_up((size_t)2 * kNumSMs * 128 * kDc * sizeof(__nv_bfloat16), 256);
 }
-size_t lse_part_bytes() { return align_up((size_t)2 * kMaxPairs * 128 * sizeof(float), 256); }
+size_t lse_part_bytes() { return align_up((size_t)2 * kNumSMs * 128 * sizeof(float), 256); }
 size_t plan_bytes(int B, int Hq) {
   return align_up(((size_t)B * Hq + 2 + Hq) * sizeof(int), 256);
 }
@@ -1342,6 +1895,24 @@ int pairs_for_device() {
   const int n = pairs_on_device();
   const int limit = g_pairs_limit.load(std::memory_order_relaxed);
   return (limit > 0 && limit < n) ? limit : n;
+}
+
+// CTAs of the few-heads kernel: one per SM (at most 148), or the test
+// hook's limit.
+int ctas_for_device() {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cached[dev] <= 0) {
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return 0;
+    }
+    cached[dev] = sms < kNumSMs ? sms : kNumSMs;
+  }
+  const int limit = g_pairs_limit.load(std::memory_order_relaxed);
+  return (limit > 0 && limit < cached[dev]) ? limit : cached[dev];
 }
 
 // Log-sum-exp merge of P pieces of the same rows (the outputs of calls over
@@ -1438,15 +2009,13 @@ cudaError_t launch_decode_tc(const void *q_lat, const void *q_rope, const void *
       !make_tmap_2d_bf16(&tm_qrope, q_rope, kDr, rows, kDr * 2, 64, 64,
                          CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  // several query slots: the slot-major plan (each slot over its own share
-  // of the pairs); one slot: items in order
-  const bool slot_major = Hq > 1;
-  auto decode_kernel = slot_major ? decode_tc_kernel<true> : decode_tc_kernel<false>;
+  // few heads: one CTA per SM, items in order; else pairs, and with several
+  // query slots the slot-major plan (each slot over its own share of the
+  // pairs)
+  const bool few_heads = d.H <= sh::kRows;
+  const bool slot_major = !few_heads && Hq > 1;
   auto combine_kernel = slot_major ? combine_tc_kernel<true> : combine_tc_kernel<false>;
-  cudaError_t e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)kSmemBytes);
-  if (e != cudaSuccess) return e;
-  const int npairs = pairs_for_device();
+  const int npairs = few_heads ? ctas_for_device() : pairs_for_device();
   if (npairs <= 0) return cudaErrorInvalidDevice;
   DecodeArgs a;
   a.q_lat = static_cast<const __nv_bfloat16 *>(q_lat);
@@ -1488,13 +2057,35 @@ cudaError_t launch_decode_tc(const void *q_lat, const void *q_rope, const void *
   pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   pdl[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * npairs, 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = st;
   cfg.attrs = pdl;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, decode_kernel, tm_cache, tm_cache_v, tm_qlat, tm_qrope, a);
+  cudaError_t e;
+  if (few_heads) {
+    // the query as 16-row boxes: one copy of 8 latent boxes and one RoPE box
+    CUtensorMap tm_q16, tm_r16;
+    if (!make_tmap_3d(&tm_q16, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, q_lat, 64, rows, kDc / 64,
+                      kDc * 2, 128, 64, sh::kRows, kDc / 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tmap_2d_bf16(&tm_r16, q_rope, kDr, rows, kDr * 2, 64, sh::kRows,
+                           CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+    e = cudaFuncSetAttribute(decode_sh_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)sh::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    cfg.gridDim = dim3(npairs, 1, 1);
+    cfg.blockDim = dim3(sh::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = sh::kSmemBytes;
+    e = cudaLaunchKernelEx(&cfg, decode_sh_kernel, tm_cache, tm_q16, tm_r16, a);
+  } else {
+    auto decode_kernel = slot_major ? decode_tc_kernel<true> : decode_tc_kernel<false>;
+    e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    cfg.gridDim = dim3(2 * npairs, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    e = cudaLaunchKernelEx(&cfg, decode_kernel, tm_cache, tm_cache_v, tm_qlat, tm_qrope, a);
+  }
   if (e != cudaSuccess) return e;
   const long rows_total = (long)B * Hq * d.H;
   cfg.gridDim = dim3((unsigned)((rows_total + kCombineRows - 1) / kCombineRows), 1, 1);

@@ -94,6 +94,9 @@ CASES = {
     "h128_mtp_causal": (128, [2, 5, 130, 777], 2, {}),
     "h128_short_rows": (128, [1, 3], 2, {}),  # seqlen < Hq leaves a row empty
     "h16_lite_like": (16, [100, 2049], 1, {}),
+    # few heads, one CTA per SM: two causal slots, and H below 16
+    "h16_mtp_causal": (16, [2, 5, 130, 777], 2, {}),
+    "h8_few_heads": (8, [1, 64, 65, 3000], 1, {}),
     "h64_odd_heads": (64, [129, 7], 1, {}),
 }
 
@@ -200,25 +203,28 @@ def _pieces(seqlens, Hq, npairs, item_cost=6, tile=64):
 
 
 SPLIT_CASES = {
-    "hq1": ([4000, 300, 64, 1, 900, 2500], 1),
-    "hq2": ([5000, 70, 5, 130], 2),
+    # name: (H, seqlens, Hq, split counts swept)
+    "hq1": (128, [4000, 300, 64, 1, 900, 2500], 1, (1, 3, 7, 74)),
+    "hq2": (128, [5000, 70, 5, 130], 2, (1, 3, 7, 74)),
+    # few heads: one CTA per SM takes the place of a pair, up to 148 of them
+    "h16": (16, [4000, 300, 64, 1, 900, 2500], 1, (1, 3, 7, 148)),
 }
 
 
 @pytest.mark.parametrize("case", sorted(SPLIT_CASES))
 def test_split_invariance(mla, case):
-    """The result does not depend on how the items are cut between CTA pairs:
-    the pair count of the split plan is swept over 1, 3, 7 and every pair,
-    which cuts the longest item into 1, 2, 3 and about twenty pieces; every
-    sweep point matches the oracle, and the points match one another within
-    the rounding of the fp32 partials."""
-    seqlens, Hq = SPLIT_CASES[case]
-    inputs = synth.random_small(seed=9, H=128, seqlens=seqlens, Hq=Hq, **DS)
+    """The result does not depend on how the items are cut between CTA pairs
+    (or, with few heads, CTAs): the split count of the plan is swept over 1,
+    3, 7 and every pair (CTA), which cuts the longest item into 1, 2, 3 and
+    about twenty (forty) pieces; every sweep point matches the oracle, and
+    the points match one another within the rounding of the fp32 partials."""
+    H, seqlens, Hq, sweep = SPLIT_CASES[case]
+    inputs = synth.random_small(seed=9, H=H, seqlens=seqlens, Hq=Hq, **DS)
     out, o_lat, lse, _ = run_oracle_step(inputs)
     results = {}
     covered = set()
     try:
-        for npairs in (1, 3, 7, 74):
+        for npairs in sweep:
             mla.mla_debug_set_decode_pairs(npairs)
             covered.add(max(_pieces(seqlens, Hq, npairs)))
             res = run_gpu_step(mla, inputs)
