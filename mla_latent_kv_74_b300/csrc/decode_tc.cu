@@ -96,6 +96,10 @@ constexpr float kRescaleThreshold = 8.0f;  // log2(256)
 // boundary get fewer tiles (6 balanced the pairs' end times best: at 7 the
 // pairs without a boundary ended last).
 constexpr int kItemCost = 6;
+// The same for the few-heads kernel (one CTA per SM), whose item start costs
+// about one tile: the query takes one ring stage and the epilogue of the
+// previous item delays the next item's first PV.
+constexpr int kShItemCost = 2;
 
 constexpr uint32_t kRankV = 0, kRankS = 1;
 constexpr uint16_t kMaskS = 1u << kRankS;
@@ -253,9 +257,9 @@ __device__ __forceinline__ bool wait_bar_warp(uint64_t *bar, uint32_t parity, vo
 // The segments of one pair: consecutive (item, tile range) pieces of its
 // range [t_begin, t_end) of the plan's order, walked from item w0 (whose
 // span starts at s0); tile counts come from seqlens.  In the plan's order an
-// item with n > 0 tiles spans kItemCost + n units, the first kItemCost
-// standing for its start-up cost and holding no tile: unit u of the span is
-// tile u - kItemCost.
+// item with n > 0 tiles spans kCost + n units, the first kCost standing for
+// its start-up cost and holding no tile: unit u of the span is tile
+// u - kCost.
 // Item of plan position u.  With one query slot the plan follows the items;
 // with several (kSlotMajor) it lists every sequence's slot 0, then every
 // sequence's slot 1, and so on.
@@ -264,7 +268,7 @@ __device__ __forceinline__ int item_at(const DecodeArgs &a, int u) {
   return kSlotMajor ? (u % a.B) * a.Hq + u / a.B : u;
 }
 
-template <bool kSlotMajor>
+template <bool kSlotMajor, int kCost = kItemCost>
 struct SegIter {
   const DecodeArgs *a;
   int W, t_begin, t_end, w, s;  // w: item (walked in plan order)
@@ -283,7 +287,7 @@ struct SegIter {
       bool bad = false;
       const int n = visible_len(*a, w, &bad);
       const int nt = (n + kTile - 1) / kTile;
-      const int st = s, e = nt > 0 ? s + kItemCost + nt : s;
+      const int st = s, e = nt > 0 ? s + kCost + nt : s;
       const int cur = w;
       if (kSlotMajor) {
         // the same slot of the next sequence; past the last sequence, the
@@ -300,8 +304,8 @@ struct SegIter {
       if (e <= st || e <= t_begin) continue;
       const int g0 = st > t_begin ? st : t_begin;
       const int g1 = e < t_end ? e : t_end;
-      const int l0 = g0 - st - kItemCost > 0 ? g0 - st - kItemCost : 0;
-      const int l1 = g1 - st - kItemCost > 0 ? g1 - st - kItemCost : 0;
+      const int l0 = g0 - st - kCost > 0 ? g0 - st - kCost : 0;
+      const int l1 = g1 - st - kCost > 0 ? g1 - st - kCost : 0;
       if (l1 <= l0) continue;  // only start-up units of this item here
       *item = cur;
       *lt0 = l0;
@@ -1236,7 +1240,7 @@ __global__ void __launch_bounds__(sh::kThreads, 1)
       const int n = visible_len(a, u, &bad);
       any_bad |= bad;
       const int nt = (n + kTile - 1) / kTile;
-      pre[u + 1] = nt > 0 ? nt + kItemCost : 0;
+      pre[u + 1] = nt > 0 ? nt + kShItemCost : 0;
     }
     if (any_bad && cta == 0) set_device_error(a.err, kDevBounds);
     __syncthreads();
@@ -1284,7 +1288,7 @@ __global__ void __launch_bounds__(sh::kThreads, 1)
   const bool bad_smem = misc->bad_smem != 0;
   const int t_begin = misc->t_begin, t_end = misc->t_end, w0 = misc->w0, s0 = misc->s0;
   MLA_TRACE_CTA(1);
-  SegIter<false> it;
+  SegIter<false, kShItemCost> it;
   it.init(&a, W, t_begin, t_end, w0, s0);
   int item, lt0, lt1, n_vis;
   bool whole;
@@ -1705,7 +1709,7 @@ __device__ __forceinline__ void load_piece16(const __nv_bfloat16 *row, int lane,
     v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
   }
 }
-template <bool kSlotMajor>
+template <bool kSlotMajor, int kCost = kItemCost>
 __global__ void __launch_bounds__(32 * kCombineRows) combine_tc_kernel(DecodeArgs a) {
   // launched early, behind the decode grid: its pieces are complete and
   // visible only after this wait; the next kernel may launch after it
@@ -1737,14 +1741,14 @@ __global__ void __launch_bounds__(32 * kCombineRows) combine_tc_kernel(DecodeArg
     const int s = pre[u] - base;
     e = pre[u + 1] - base;
     if (e <= s) return;
-    f = s + kItemCost;
+    f = s + kCost;
     grp_pair0 = grp * (a.npairs / ngroups);
   } else {
     per = a.plan[0];
     const int s = a.plan[1 + w];
     e = a.plan[2 + w];
     if (e <= s) return;
-    f = s + kItemCost;
+    f = s + kCost;
     grp_pair0 = 0;
   }
   if (per <= 0) return;
@@ -2014,7 +2018,9 @@ cudaError_t launch_decode_tc(const void *q_lat, const void *q_rope, const void *
   // pairs)
   const bool few_heads = d.H <= sh::kRows;
   const bool slot_major = !few_heads && Hq > 1;
-  auto combine_kernel = slot_major ? combine_tc_kernel<true> : combine_tc_kernel<false>;
+  auto combine_kernel = few_heads    ? combine_tc_kernel<false, kShItemCost>
+                        : slot_major ? combine_tc_kernel<true>
+                                     : combine_tc_kernel<false>;
   const int npairs = few_heads ? ctas_for_device() : pairs_for_device();
   if (npairs <= 0) return cudaErrorInvalidDevice;
   DecodeArgs a;

@@ -203,22 +203,23 @@ def _pieces(seqlens, Hq, npairs, item_cost=6, tile=64):
 
 
 SPLIT_CASES = {
-    # name: (H, seqlens, Hq, split counts swept)
-    "hq1": (128, [4000, 300, 64, 1, 900, 2500], 1, (1, 3, 7, 74)),
-    "hq2": (128, [5000, 70, 5, 130], 2, (1, 3, 7, 74)),
+    # name: (H, seqlens, Hq, split counts swept, start-up units per item)
+    "hq1": (128, [4000, 300, 64, 1, 900, 2500], 1, (1, 3, 7, 74), 6),
+    "hq2": (128, [5000, 70, 5, 130], 2, (1, 3, 7, 74), 6),
     # few heads: one CTA per SM takes the place of a pair, up to 148 of them
-    "h16": (16, [4000, 300, 64, 1, 900, 2500], 1, (1, 3, 7, 148)),
+    "h16": (16, [4000, 300, 64, 1, 900, 2500], 1, (1, 5, 7, 148), 2),
 }
 
 
 @pytest.mark.parametrize("case", sorted(SPLIT_CASES))
 def test_split_invariance(mla, case):
     """The result does not depend on how the items are cut between CTA pairs
-    (or, with few heads, CTAs): the split count of the plan is swept over 1,
-    3, 7 and every pair (CTA), which cuts the longest item into 1, 2, 3 and
-    about twenty (forty) pieces; every sweep point matches the oracle, and
-    the points match one another within the rounding of the fp32 partials."""
-    H, seqlens, Hq, sweep = SPLIT_CASES[case]
+    (or, with few heads, CTAs): the split count of the plan is swept from 1
+    to every pair (CTA), which cuts the longest item into 1, 2 or more, 3 or
+    more and twenty to sixty pieces; every sweep point matches the oracle,
+    and the points match one another within the rounding of the fp32
+    partials."""
+    H, seqlens, Hq, sweep, cost = SPLIT_CASES[case]
     inputs = synth.random_small(seed=9, H=H, seqlens=seqlens, Hq=Hq, **DS)
     out, o_lat, lse, _ = run_oracle_step(inputs)
     results = {}
@@ -226,7 +227,7 @@ def test_split_invariance(mla, case):
     try:
         for npairs in sweep:
             mla.mla_debug_set_decode_pairs(npairs)
-            covered.add(max(_pieces(seqlens, Hq, npairs)))
+            covered.add(max(_pieces(seqlens, Hq, npairs, item_cost=cost)))
             res = run_gpu_step(mla, inputs)
             assert res["status"] == 0
             compare(res["o_lat"], o_lat, f"o_lat pairs={npairs}")
