@@ -67,6 +67,10 @@
 //
 // Every wait is bounded; a lost wait records MLA_ERR_TIMEOUT in the
 // workspace, tells the peer CTA to stop, and the CTA unwinds (no trap).
+//
+// With at most 16 heads (the DeepSeek-V2-Lite shape) decode_sh_kernel
+// replaces the pair: O kept transposed fits one SM's TMEM next to the
+// query, so every SM streams its own tiles (see its own comment below).
 #include <math.h>
 
 #include <atomic>
