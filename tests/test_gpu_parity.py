@@ -251,6 +251,42 @@ def test_deterministic(mla):
         assert np.array_equal(a[k], b[k]), k
 
 
+def test_few_heads_workspace_reuse(mla):
+    """One workspace reused for several few-heads calls (one CTA per SM),
+    with the split count changed between them, gives the same bytes for the
+    same split every time, and every call matches the oracle."""
+    inputs = synth.random_small(seed=14, H=16, seqlens=[1500, 65, 1, 700], Hq=1, **DS)
+    dev = to_device(inputs)
+    d = dims_for(mla, inputs)
+    B, Hq, H, _ = dev["q_nope"].shape
+    ms = int(inputs["seqlens"].max())
+    q_lat = torch.empty(B, Hq, H, d.d_c, dtype=torch.bfloat16, device="cuda")
+    mla.mla_absorb_query(dev["q_nope"], dev["W_UK"], q_lat, d)
+    ws = mla.alloc_workspace(B, Hq, ms, d)
+    outs = []
+    try:
+        for npairs in (0, 9, 0, 0):
+            mla.mla_debug_set_decode_pairs(npairs)
+            o = torch.empty(B, Hq, H, d.d_c, dtype=torch.bfloat16, device="cuda")
+            lse = torch.empty(B, Hq, H, dtype=torch.float32, device="cuda")
+            mla.mla_decode(q_lat, dev["q_rope"], dev["cache"], inputs["num_blocks"],
+                           dev["block_table"], dev["seqlens"], ms, d, o, lse, ws)
+            assert mla.mla_get_error(ws) == 0
+            outs.append((o.float().cpu().numpy(), lse.cpu().numpy()))
+    finally:
+        mla.mla_debug_set_decode_pairs(0)
+    for k in (2, 3):
+        assert np.array_equal(outs[k][0], outs[0][0]) and np.array_equal(outs[k][1], outs[0][1])
+    compare(outs[1][0], outs[0][0], "o_lat, 9 CTAs vs all")
+    compare(outs[1][1], outs[0][1], "lse, 9 CTAs vs all")
+    _, o_ref, lse_ref = omla.mla_decode(f64(inputs["q_nope"]), f64(inputs["q_rope"]),
+                                        f64(inputs["cache"]), inputs["block_table"].numpy(),
+                                        inputs["seqlens"].numpy(), f64(inputs["W_UK"]),
+                                        f64(inputs["W_UV"]), Hq)
+    compare(outs[0][0], o_ref, "o_lat")
+    compare(outs[0][1], lse_ref, "lse")
+
+
 def test_bad_block_index_reported(mla):
     """A table entry outside [0, num_blocks) is flagged on the device; that
     sequence's rows come back as 0 / -inf and the others are untouched."""
