@@ -94,20 +94,23 @@ def _oracle(inputs, ranges):
 
 
 CASES = {
+    # name: (H, seqlens, Hq, ranges)
     # one long sequence cut into three ranks' ranges (each range itself cut
     # between several CTA pairs), plus short ones that end inside a range
-    "long_three": ([5000, 70, 900], 1, [(0, 20), (20, 55), (55, BIG)]),
+    "long_three": (128, [5000, 70, 900], 1, [(0, 20), (20, 55), (55, BIG)]),
     # two query slots (causal), four ranges, one of them past every sequence
-    "mtp_four": ([3000, 130, 64], 2, [(0, 1), (1, 2), (2, 40), (40, 100)]),
+    "mtp_four": (128, [3000, 130, 64], 2, [(0, 1), (1, 2), (2, 40), (40, 100)]),
     # ranges of one block each at the start, then the rest
-    "small_blocks": ([700, 65], 1, [(0, 1), (1, 2), (2, 3), (3, BIG)]),
+    "small_blocks": (128, [700, 65], 1, [(0, 1), (1, 2), (2, 3), (3, BIG)]),
+    # few heads (one CTA per SM): two ranks' ranges, two query slots
+    "few_heads": (16, [4000, 129, 1], 2, [(0, 30), (30, BIG)]),
 }
 
 
 @pytest.mark.parametrize("case", sorted(CASES))
 def test_block_pieces_and_merge(mla, case):
-    seqlens, Hq, ranges = CASES[case]
-    inputs = synth.random_small(seed=21, H=128, seqlens=seqlens, Hq=Hq, **DS)
+    H, seqlens, Hq, ranges = CASES[case]
+    inputs = synth.random_small(seed=21, H=H, seqlens=seqlens, Hq=Hq, **DS)
     res = _gpu(mla, inputs, ranges)
     assert res["status"] == 0
     pieces, (o_ref, lse_ref) = _oracle(inputs, ranges)
@@ -121,9 +124,10 @@ def test_block_pieces_and_merge(mla, case):
     compare(res["lse_m"], res["lse_full"], "merged vs mla_decode lse")
 
 
-def test_whole_range_is_the_decode(mla):
+@pytest.mark.parametrize("H", [128, 16])
+def test_whole_range_is_the_decode(mla, H):
     """[0, INT_MAX) is the same computation as mla_decode: identical bytes."""
-    inputs = synth.random_small(seed=22, H=128, seqlens=[2000, 1, 300], Hq=1, **DS)
+    inputs = synth.random_small(seed=22, H=H, seqlens=[2000, 1, 300], Hq=1, **DS)
     res = _gpu(mla, inputs, [(0, BIG)])
     assert res["status"] == 0
     assert np.array_equal(res["o_p"][0], res["o_full"])
