@@ -190,8 +190,8 @@ struct DecodeArgs {
   float scale_log2;
   __nv_bfloat16 *o_lat;
   float *lse;
-  __nv_bfloat16 *o_part;  // [2 * kMaxPairs][128][512] (O / l of split pieces)
-  float *lse_part;  // [2 * kMaxPairs][128]
+  __nv_bfloat16 *o_part;  // [2 * pairs or CTAs][128][512] (O / l of split pieces)
+  float *lse_part;  // [2 * pairs or CTAs][128]
   // plan: [0] = number of slot groups G (1 or Hq), [1+g] = units per pair of
   // group g, [1+Hq+u] = prefix of units per item in plan order u (u = slot *
   // B + b for item b * Hq + slot), u = 0..W
@@ -1857,11 +1857,12 @@ __global__ void __launch_bounds__(32 * kCombineRows) combine_tc_kernel(DecodeArg
   if (lane == 0) a.lse[rowg] = mx + logf(sum);
 }
 
-// Two piece slots per pair, or per CTA of the few-heads kernel.
-size_t part_bytes() {
-  return align_up((size_t)2 * kNumSMs * 128 * kDc * sizeof(__nv_bfloat16), 256);
+// Two piece slots of 128 rows per pair, or per CTA of the few-heads kernel.
+size_t piece_slots(int H) { return (size_t)2 * (H <= sh::kRows ? kNumSMs : kMaxPairs); }
+size_t part_bytes(int H) {
+  return align_up(piece_slots(H) * 128 * kDc * sizeof(__nv_bfloat16), 256);
 }
-size_t lse_part_bytes() { return align_up((size_t)2 * kNumSMs * 128 * sizeof(float), 256); }
+size_t lse_part_bytes(int H) { return align_up(piece_slots(H) * 128 * sizeof(float), 256); }
 size_t plan_bytes(int B, int Hq) {
   return align_up(((size_t)B * Hq + 2 + Hq) * sizeof(int), 256);
 }
@@ -1991,8 +1992,8 @@ bool tc_decode_supported(const mla_dims &d, int B, int Hq) {
          d.H <= 128 && (long)B * Hq <= kMaxItems;
 }
 
-size_t tc_decode_workspace_bytes(int B, int Hq, const mla_dims &) {
-  return kWsHeader + part_bytes() + lse_part_bytes() + plan_bytes(B, Hq);
+size_t tc_decode_workspace_bytes(int B, int Hq, const mla_dims &d) {
+  return kWsHeader + part_bytes(d.H) + lse_part_bytes(d.H) + plan_bytes(B, Hq);
 }
 
 cudaError_t launch_decode_tc(const void *q_lat, const void *q_rope, const void *cache,
@@ -2053,8 +2054,8 @@ cudaError_t launch_decode_tc(const void *q_lat, const void *q_rope, const void *
   a.lse = lse;
   a.err = reinterpret_cast<int *>(ws);
   a.o_part = o_part;
-  a.lse_part = reinterpret_cast<float *>(ws + kWsHeader + part_bytes());
-  a.plan = reinterpret_cast<int *>(ws + kWsHeader + part_bytes() + lse_part_bytes());
+  a.lse_part = reinterpret_cast<float *>(ws + kWsHeader + part_bytes(d.H));
+  a.plan = reinterpret_cast<int *>(ws + kWsHeader + part_bytes(d.H) + lse_part_bytes(d.H));
 #ifdef MLA_TRACE
   {
     const unsigned long long init[2] = {~0ull, 0ull};
