@@ -1158,7 +1158,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 // TMEM); P (16 rows x 64 tokens, bf16) goes to shared memory as the K-major
 // B operand of the PV MMAs, whose A operand is the same ring stage read
 // MN-major (latent contiguous).  The plan, the pieces and the combine are
-// the pair kernel's, with one CTA in the place of a pair.
+// the pair kernel's, with one CTA in the place of a pair and an item start
+// charged as kShItemCost tiles.
 //
 // Warp roles (288 threads): warp 0 TMA producer; warps 1 and 2 QK^T issuers
 // (even / odd tiles); warp 3 TMEM owner and PV issuer; warps 4-7 rescale
@@ -1346,7 +1347,7 @@ __global__ void __launch_bounds__(sh::kThreads, 1)
       for (int k = r - kStages < 0 ? 0 : r - kStages; k < r; ++k)
         wait_bar_warp(&bars->empty[k % kStages], (k / kStages) & 1, abort);
   } else if (warp == 1 || warp == 2) {
-    // ========== QK^T issuers: warp 1 even tiles, warp 6 odd ==========
+    // ========== QK^T issuers: warp 1 even tiles, warp 2 odd ==========
     if (lane == 0) {
       const int mine = warp - 1;
       const uint32_t idesc = ptx::idesc_bf16(128, kTile, false, false);
