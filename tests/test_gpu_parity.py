@@ -96,6 +96,7 @@ CASES = {
     "h16_lite_like": (16, [100, 2049], 1, {}),
     # few heads, one CTA per SM: two causal slots, and H below 16
     "h16_mtp_causal": (16, [2, 5, 130, 777], 2, {}),
+    "h16_short_rows": (16, [1, 3, 70], 2, {}),  # seqlen < Hq leaves a row empty
     "h8_few_heads": (8, [1, 64, 65, 3000], 1, {}),
     "h64_odd_heads": (64, [129, 7], 1, {}),
 }
@@ -287,10 +288,11 @@ def test_few_heads_workspace_reuse(mla):
     compare(outs[0][1], lse_ref, "lse")
 
 
-def test_bad_block_index_reported(mla):
+@pytest.mark.parametrize("H", [128, 16])
+def test_bad_block_index_reported(mla, H):
     """A table entry outside [0, num_blocks) is flagged on the device; that
     sequence's rows come back as 0 / -inf and the others are untouched."""
-    inputs = synth.random_small(seed=12, H=128, seqlens=[130, 200], Hq=1, **DS)
+    inputs = synth.random_small(seed=12, H=H, seqlens=[130, 200], Hq=1, **DS)
     good = run_gpu_step(mla, inputs)
     bad = dict(inputs)
     bt = inputs["block_table"].clone()
