@@ -102,7 +102,10 @@ def test_noalloc_fits_every_tensor_core_workload():
     lib = m.raw_lib()
     n = ctypes.c_size_t()
     for H, B, Hq, max_seqlen in ((16, 32, 1, 4096), (128, 64, 1, 8192), (128, 128, 2, 32768),
-                                 (128, 4, 1, 131072)):
+                                 (128, 4, 1, 131072),
+                                 # the most items the tensor-core plan takes, with
+                                 # few heads (two piece slots per SM) and with pairs
+                                 (16, 8192, 1, 64), (128, 4096, 2, 64)):
         assert lib.mla_decode_workspace_size(B, Hq, max_seqlen, ctypes.byref(_dims(H=H)),
                                              ctypes.byref(n)) == m.MLA_OK
         assert n.value <= m.NOALLOC_SCRATCH_BYTES, (H, B, Hq, n.value)
