@@ -110,6 +110,17 @@ def test_bf16_deepseek_dims(mla, name):
     _check_step(res, inputs, "bf16")
 
 
+@pytest.mark.parametrize("H", [8, 32])
+def test_single_sequence_few_rows(mla, H):
+    """One sequence, one slot: fewer query rows in all (H) than the query
+    copy's box (16 rows with few heads, 64 in the pair kernel); the rows past
+    the tensor read as zero."""
+    inputs = synth.random_small(seed=15, H=H, seqlens=[300], Hq=1, **DS)
+    res = run_gpu_step(mla, inputs)
+    assert res["status"] == 0
+    _check_step(res, inputs, "bf16")
+
+
 @pytest.mark.parametrize("shape", [
     dict(H=3, d_h=40, d_c=72, d_r=16, bs=16, dtype=torch.bfloat16),
     dict(H=8, d_h=32, d_c=64, d_r=32, bs=32, dtype=torch.float32),
